@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of the Mamba-2 SSD forward scan on B300: tokens/s and effective TFLOP/s against
+the HBM / bf16 roofline, with the CPU oracle timed beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload I]
+
+One step = one ssd_scan_fwd call over the whole workload (all four steps of the scan: chunk
+cumsum and decay, intra-chunk GEMMs and chunk states, inter-chunk recurrence, off-diagonal
+output with the skip term and the store).  Rank 0 prints one JSON line.
+
+Under torchrun every rank scans its own full copy of the workload (the path shards into
+independent (batch, head) problems; there is no data-path collective), so scaling is weak and
+``value`` is the tokens all ranks processed divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SSD scan fwd tokens/s and TFLOP/s on 1 B300; % of roofline (bf16 MMA vs HBM)"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ---------------------------------------------------------------- algorithmic work model --
+
+def algorithmic_bytes(w, with_h0: bool, with_D: bool = True) -> int:
+    """Bytes the method must move: inputs once, outputs once (chunk states excluded)."""
+    eb = 4 if w.dtype == "f32" else 2
+    b, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    n = eb * (2 * b * L * H * P + b * L * H + 2 * b * L * G * N)   # x, y, dt, B, C
+    n += 4 * H * (2 if with_D else 1)                                # A, D
+    n += 4 * b * H * P * N * (2 if with_h0 else 1)                  # final (+ initial) state
+    return n
+
+
+def algorithmic_flops(w) -> int:
+    """FLOPs of the chunk algorithm with full Q x Q tiles, per (b, h, chunk):
+    2Q^2P (Y_diag) + 2QPN (chunk state) + 2QNP (off-diagonal) + 2Q^2N/R (C B^T, shared by the
+    R heads of a group) + 2PN (state recurrence) + 2QP (skip term)."""
+    b, L, H, P, N, G, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk
+    R = H // G
+    nc = math.ceil(L / Q)
+    per = 2 * Q * Q * P + 2 * Q * P * N + 2 * Q * N * P + 2 * Q * Q * N / R + 2 * P * N + 2 * Q * P
+    return int(b * H * nc * per)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mamba_ssd_scan_05_b300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[f"{kernel}|{workload}"]
+        if e.get("source_sha") != kernel_source_sha():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------- clock sampling --
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background (read only)."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.gpu_index = gpu_index
+        self.interval_ms = interval_ms
+        self.samples = []        # (t, sm_mhz, max_mhz, reasons set)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={self.interval_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}
+            self.samples.append((time.time(), sm, mx, reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not win:   # region shorter than the sampling interval: nearest samples around it
+            win = sorted(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[:3]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted(set().union(*[s[3] for s in win]))
+        return {"sm_mhz": statistics.median(s[1] for s in win),
+                "sm_max_mhz": max(s[2] for s in win), "reasons": reasons,
+                "samples": len(win)}
+
+
+# ------------------------------------------------------------------------------ oracle leg --
+
+def oracle_sample_rate(w, inp, budget_s: float = 8.0, n_threads: int = 0):
+    """Time the oracle (as it stands) on a bounded sample of (b, h) problems of the workload.
+
+    Returns (tokens_per_s, threads_used, description).  One token = one sequence position of
+    one batch row with all H heads, so k sampled heads of length L count as k * L / H tokens.
+    """
+    import oracle
+    b, H, L = w.batch, w.nheads, w.seqlen
+    cores = os.cpu_count() or 1
+    # calibrate on one head, then size the sample to the budget
+    heads_all = [(bb, hh) for bb in range(b) for hh in range(H)]
+    probe = heads_all[:1]
+    _, xs, dts, As, Bs, Cs, Ds, h0s = oracle.gather_problems(
+        inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"], probe)
+    t0 = time.perf_counter()
+    oracle.scan_problems(xs, dts, As, Bs, Cs, Ds, h0s, n_threads=1)
+    per_head = max(time.perf_counter() - t0, 1e-6)
+    k = max(1, min(len(heads_all), int(budget_s * cores / per_head)))
+    k = max(1, (k // cores) * cores) if k >= cores else k
+    heads = heads_all[:k]
+    _, xs, dts, As, Bs, Cs, Ds, h0s = oracle.gather_problems(
+        inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"], heads)
+    t0 = time.perf_counter()
+    _, _, used = oracle.scan_problems(xs, dts, As, Bs, Cs, Ds, h0s, n_threads=n_threads)
+    dt_s = time.perf_counter() - t0
+    tokens = k * L / H
+    desc = (f"{k} of {len(heads_all)} (batch, head) problems, full length L={L}, "
+            f"{dt_s:.2f} s; tokens counted as k*L/H")
+    return tokens / dt_s, used, desc, dt_s
+
+
+# --------------------------------------------------------------------------------- main --
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload_config(w, extra: dict) -> dict:
+    cfg = {"workload": w.describe(), "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+           "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk}
+    cfg.update(extra)
+    return cfg
+
+
+def run_reference(args, w, ws, rank):
+    """The reference arm: the CPU oracle as it stands, on the host cores, rank 0 only."""
+    if rank != 0:
+        return 0
+    from mamba_ssd_scan_05_b300 import workloads
+    inp = workloads.make_inputs(w)
+    rates = []
+    used = 1
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        budget = max(0.5, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+        r, used, desc, _ = oracle_sample_rate(w, inp, budget_s=budget)
+        if i >= args.warmup:
+            rates.append(r)
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * (w.tokens / value), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, {"l2": "n/a (CPU)"}),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2,
+                    help="workload index 0-4 (default 2: the Mamba-2-2.7B-shaped layer)")
+    ap.add_argument("--path", type=int, default=-1, help="kernel family (-1 auto, 0 chunked, 1 tc)")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from mamba_ssd_scan_05_b300 import workloads
+    w = workloads.WORKLOADS[args.workload]
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, w, ws, rank)
+
+    import torch
+    import torch.distributed as dist
+    import mamba_ssd_scan_05_b300 as m
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    # inputs: enough distinct sets that consecutive steps never find theirs in L2
+    inp = workloads.make_inputs(w)
+    with_h0 = inp["h0"] is not None
+    set_bytes = algorithmic_bytes(w, with_h0)
+    n_sets = max(2, math.ceil(3 * L2_BYTES / set_bytes))
+    sets = []
+    for s in range(n_sets):
+        src = inp if s == 0 else workloads.make_inputs(w, seed=w.seed + 7919 * s)
+        d = {k: (None if v is None else v.to(dev)) for k, v in src.items()}
+        d["y"] = torch.empty_like(d["x"])
+        d["hT"] = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32,
+                              device=dev)
+        sets.append(d)
+    dims = m.make_dims(sets[0]["x"], sets[0]["B"])
+    path = m.ssd_scan_resolve_path(dims, w.chunk, args.path)
+    if path < 0:
+        raise SystemExit(f"workload not supported: {m.ssd_scan_strerror(-path)}")
+    wsb = m.ssd_scan_workspace_bytes(dims, w.chunk, path)
+    workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    launches_per_call = {m.SSD_PATH_CHUNKED: 3, m.SSD_PATH_TC: 1}[path]
+
+    def step(i):
+        d = sets[i % n_sets]
+        m.ssd_scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"],
+                       chunk_size=w.chunk, path=args.path, y=d["y"], final_state=d["hT"],
+                       workspace=workspace)
+
+    stream = torch.cuda.current_stream(dev)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if m.ssd_scan_get_status(workspace) != 0:
+        raise SystemExit("device status error during warm-up")
+
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(args.warmup + i)
+        ends[i].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    wall1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    status = m.ssd_scan_get_status(workspace)
+    total_ms = ev0.elapsed_time(ev1)
+    call_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens_all = w.tokens * ws
+    value = tokens_all / (total_ms / 1e3 / args.steps) / 1.0
+
+    # end to end through the host-buffer entry point (pinned host memory, copies timed)
+    e2e = None
+    if args.e2e_steps > 0:
+        pinned = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+        y_h = torch.empty_like(pinned["x"], pin_memory=True)
+        h_h = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32,
+                          pin_memory=True)
+        arena = torch.empty(m.ssd_scan_host_arena_bytes(dims, w.chunk), dtype=torch.uint8,
+                            device=dev)
+        args_h = (pinned["x"], pinned["dt"], pinned["A"], pinned["B"], pinned["C"],
+                  pinned["D"], pinned["h0"])
+        m.ssd_scan_fwd_host(*args_h, chunk_size=w.chunk, y=y_h, final_state=h_h, arena=arena,
+                            device=dev)
+        if ws > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            m.ssd_scan_fwd_host(*args_h, chunk_size=w.chunk, y=y_h, final_state=h_h,
+                                arena=arena, device=dev)
+        t_e2e = time.perf_counter() - t0
+        if ws > 1:
+            t = torch.tensor([t_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
+        d2h = y_h.numel() * y_h.element_size() + h_h.numel() * h_h.element_size()
+        e2e = {"value": tokens_all * args.e2e_steps / t_e2e, "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    nbytes = algorithmic_bytes(w, with_h0)
+    flops = algorithmic_flops(w)
+    avg_call_s = statistics.mean(call_ms) / 1e3
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    kernel = {m.SSD_PATH_CHUNKED: "chunk_output_kernel", m.SSD_PATH_TC: "ssd_tc_kernel"}[path]
+    traffic = committed_traffic(kernel, w.name)
+    if bound == "hbm":
+        achieved, peak, unit = nbytes / avg_call_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = flops / avg_call_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
+                "t_roof_us": 1e6 * max(t_hbm, t_tc),
+                "roof_frac": max(t_hbm, t_tc) / avg_call_s,
+                "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                "kernel": kernel, "timed": "whole ssd_scan_fwd call (status memset + kernels)"}
+
+    cpu = None
+    if not args.no_cpu_baseline and ws >= 1:
+        r, used, desc, _ = oracle_sample_rate(w, inp)
+        cpu = {"value": r, "unit": "tokens/s", "cores": used, "kind": "oracle", "sample": desc}
+
+    clocks = sampler.summary(wall0, wall1)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": workload_config(w, {
+            "l2": f"inputs larger than L2: {n_sets} rotating input sets of {set_bytes / 1e6:.0f} MB",
+            "path": m.PATH_NAMES[path], "parallelism": f"replicas x{ws}"}),
+        "tflops_effective": flops / (total_ms / 1e3 / args.steps) / 1e12,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_call * args.steps,
+        "clocks": clocks,
+        "device_status": status,
+        "per_call_ms": {"median": statistics.median(call_ms), "min": min(call_ms),
+                        "max": max(call_ms)},
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,149 @@
+/*
+ * ssd_scan.h -- C ABI of libssd_scan.so, the B300 (sm_103a) Mamba-2 SSD forward scan.
+ *
+ * The operation (per batch row b and head h, tokens t = 0..L-1, state h_t a P x N matrix):
+ *
+ *     h_t = exp(dt_t * A_h) * h_{t-1} + dt_t * x_t B_t^T
+ *     y_t = C_t^T h_t + D_h * x_t                     (y_t[p] = sum_n C_t[n] h_t[p][n] + D_h x_t[p])
+ *
+ * with h_{-1} = initial_state (or zeros) and final_state = h_{L-1}.  Sources:
+ *   - youngju.dev "Mamba / selective SSM" article, section "LTIからSelectionへの切り替え":
+ *     Abar_t = exp(Delta_t A), Bbar_t = Delta_t B_t, h_t = Abar_t h_{t-1} + Bbar_t x_t, y_t = C_t h_t;
+ *     the SelectiveSSM listing of the same article adds the skip term D * x.
+ *   - Qiita "Mamba-2 / SSD" article, section 4.2: A = -exp(A_log) is one scalar per head, and the
+ *     scan is computed by the SSD chunk algorithm (matmuls inside a chunk, a scan between chunks)
+ *     with a chunk_size argument; section 4.1: heads as in attention, B/C shared by head groups.
+ *   - youngju.dev article, section "State Space Dualityの発見": the same y as y = M x with the
+ *     semiseparable M_ij = C_i^T Abar_{i:j} Bbar_j (i >= j); section "SSDアルゴリズムとチャンク分割":
+ *     the chunk split, the cumulative-sum decay mask and the intra-chunk dual form.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are dense, row-major, contiguous, and live in DEVICE memory unless a function
+ *     says otherwise.  The library never allocates device memory except inside the functions
+ *     whose comment says so (none here do); the caller owns every buffer.
+ *   - Layouts (T = the element type named by ssd_dims.dtype):
+ *       x              [batch, seqlen, nheads, headdim]   T
+ *       dt             [batch, seqlen, nheads]            T   (already positive: post-softplus)
+ *       A              [nheads]                           float32 (normally < 0)
+ *       B, C           [batch, seqlen, ngroups, dstate]   T
+ *       D              [nheads]                           float32, or NULL for no skip term
+ *       initial_state  [batch, nheads, headdim, dstate]   float32, or NULL for zeros
+ *       y              [batch, seqlen, nheads, headdim]   T   (written)
+ *       final_state    [batch, nheads, headdim, dstate]   float32 (written), or NULL
+ *     Head h reads B/C group h / (nheads / ngroups).
+ *   - Base pointers of x, dt, B, C, y must be 16-byte aligned; initial_state and final_state
+ *     4-byte aligned; workspace 256-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every
+ *     launch and copy is enqueued on it; the functions return without synchronising, except
+ *     ssd_scan_get_status, which synchronises `stream`.
+ *   - Errors: argument and shape errors are returned synchronously, before anything is
+ *     enqueued.  No C++ exception crosses this boundary.  A device-side bounded wait that runs
+ *     out sets an error word in the workspace; read it with ssd_scan_get_status.
+ *   - Calls on different streams may run concurrently if each has its own workspace.
+ */
+#ifndef SSD_SCAN_H_
+#define SSD_SCAN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of x, dt, B, C and y.  Arithmetic is float32 on the device in both cases. */
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+/* Problem shape.  All sizes are element counts. */
+typedef struct {
+    int64_t batch;    /* b  >= 1 */
+    int64_t seqlen;   /* L  >= 0 (0: nothing to scan; final_state = initial_state) */
+    int64_t nheads;   /* H  >= 1 */
+    int64_t headdim;  /* P  >= 1 */
+    int64_t dstate;   /* N  >= 1 */
+    int64_t ngroups;  /* G  >= 1, H % G == 0 */
+    int32_t dtype;    /* ssd_dtype */
+} ssd_dims;
+
+/* Return codes. */
+enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID = 1,      /* bad pointer, alignment, size or shape */
+    SSD_ERR_UNSUPPORTED = 2,  /* valid problem that no kernel of this build handles */
+    SSD_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, copy, attribute) */
+    SSD_ERR_TIMEOUT = 4,      /* a device-side bounded wait gave up (see ssd_scan_get_status) */
+    SSD_ERR_WORKSPACE = 5     /* workspace NULL or smaller than ssd_scan_workspace_bytes */
+};
+
+/* Kernel family.  SSD_PATH_AUTO picks: bf16 with headdim % 64 == 0 and dstate in {128, 256}
+ * -> SSD_PATH_TC (tcgen05 tensor cores, TMA, TMEM); everything else -> SSD_PATH_CHUNKED
+ * (float32 CUDA-core kernels that follow the chunk algorithm with the caller's chunk_size). */
+enum { SSD_PATH_AUTO = -1, SSD_PATH_CHUNKED = 0, SSD_PATH_TC = 1 };
+
+/* Which kernel family `path` (SSD_PATH_AUTO or explicit) resolves to for this problem, or a
+ * negative SSD_ERR_* code if the problem is invalid or the explicit path cannot run it. */
+int ssd_scan_resolve_path(const ssd_dims* dims, int chunk_size, int path);
+
+/* Device workspace bytes ssd_scan_fwd needs for this problem and path (0 on invalid input).
+ * The workspace holds a status word, per-chunk float32 states for the chunked path, and the
+ * cross-block state hand-off slots of the tensor-core path.  Its contents need no
+ * initialisation; calls sharing one workspace must be ordered on one stream. */
+size_t ssd_scan_workspace_bytes(const ssd_dims* dims, int chunk_size, int path);
+
+/*
+ * ssd_scan_fwd -- y and final_state of the scan defined above, enqueued on `stream`.
+ *
+ * chunk_size: the chunk length Q of the SSD chunk algorithm, 1 <= Q <= 256.  The result does
+ * not depend on Q beyond rounding (the chunk algorithm is exact); the chunked path cuts the
+ * sequence at multiples of Q, the tensor-core path evaluates each Q-chunk in 128-token tiles.
+ * A sequence length that is not a multiple of Q ends in a partial chunk (treated as padding
+ * tokens with dt = 0; no y is written for them).
+ *
+ * Returns SSD_OK once all work is enqueued, or an SSD_ERR_* code (nothing enqueued).
+ */
+int ssd_scan_fwd(const ssd_dims* dims,
+                 const void* x, const void* dt, const float* A,
+                 const void* B, const void* C, const float* D,
+                 const float* initial_state, int chunk_size,
+                 void* y, float* final_state,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* ssd_scan_fwd with an explicit kernel family (SSD_PATH_*).  Returns SSD_ERR_UNSUPPORTED if
+ * that family cannot run the problem. */
+int ssd_scan_fwd_path(const ssd_dims* dims,
+                      const void* x, const void* dt, const float* A,
+                      const void* B, const void* C, const float* D,
+                      const float* initial_state, int chunk_size,
+                      void* y, float* final_state,
+                      void* workspace, size_t workspace_bytes, void* stream, int path);
+
+/*
+ * Host-buffer variant: every tensor argument is a HOST pointer (page-locked memory makes the
+ * copies asynchronous), and `device_arena` is a caller-owned device buffer of at least
+ * ssd_scan_host_arena_bytes(dims, chunk_size) bytes (256-byte aligned).  Enqueues on `stream`:
+ * one host-to-device copy per input, the scan, one device-to-host copy per output.  The host
+ * outputs are valid after the caller synchronises `stream`.  Same errors as ssd_scan_fwd.
+ */
+size_t ssd_scan_host_arena_bytes(const ssd_dims* dims, int chunk_size);
+int ssd_scan_fwd_host(const ssd_dims* dims,
+                      const void* x, const void* dt, const float* A,
+                      const void* B, const void* C, const float* D,
+                      const float* initial_state, int chunk_size,
+                      void* y, float* final_state,
+                      void* device_arena, size_t arena_bytes, void* stream);
+
+/* Synchronise `stream`, then read and clear the device status word of `workspace` (the first
+ * 4 bytes).  Returns SSD_OK, SSD_ERR_TIMEOUT if a bounded device wait gave up in a call that
+ * used this workspace, or SSD_ERR_CUDA if synchronisation or the read failed. */
+int ssd_scan_get_status(void* workspace, void* stream);
+
+/* Static description of a return code. */
+const char* ssd_scan_strerror(int code);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int ssd_scan_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_SCAN_H_ */

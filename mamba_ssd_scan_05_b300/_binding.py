@@ -1,0 +1,214 @@
+"""ctypes binding of libssd_scan.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (include/ssd_scan.h).  Torch
+is used for device memory and the current stream; all computation happens in the library's
+CUDA kernels.  If the library is missing the import of a function fails loudly: there is no
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssd_scan.so")
+
+SSD_F32, SSD_BF16 = 0, 1
+SSD_OK, SSD_ERR_INVALID, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT, SSD_ERR_WORKSPACE = range(6)
+SSD_PATH_AUTO, SSD_PATH_CHUNKED, SSD_PATH_TC = -1, 0, 1
+PATH_NAMES = {SSD_PATH_CHUNKED: "chunked", SSD_PATH_TC: "tc"}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class ssd_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("nheads", ctypes.c_int64), ("headdim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+                ("dtype", ctypes.c_int32)]
+
+
+class SSDError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {ssd_scan_strerror(code)} (code {code})")
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libssd_scan.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise ImportError(f"libssd_scan.so not built at {path}; run __graft_entry__.build() "
+                              "or python -m mamba_ssd_scan_05_b300.build")
+        lib = ctypes.CDLL(path)
+        vp, sz, i32, fp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p
+        dims_p = ctypes.POINTER(ssd_dims)
+        lib.ssd_scan_resolve_path.argtypes = [dims_p, i32, i32]
+        lib.ssd_scan_resolve_path.restype = i32
+        lib.ssd_scan_workspace_bytes.argtypes = [dims_p, i32, i32]
+        lib.ssd_scan_workspace_bytes.restype = sz
+        fwd_args = [dims_p, vp, vp, fp, vp, vp, fp, fp, i32, vp, fp, vp, sz, vp]
+        lib.ssd_scan_fwd.argtypes = fwd_args
+        lib.ssd_scan_fwd.restype = i32
+        lib.ssd_scan_fwd_path.argtypes = fwd_args + [i32]
+        lib.ssd_scan_fwd_path.restype = i32
+        lib.ssd_scan_host_arena_bytes.argtypes = [dims_p, i32]
+        lib.ssd_scan_host_arena_bytes.restype = sz
+        lib.ssd_scan_fwd_host.argtypes = fwd_args
+        lib.ssd_scan_fwd_host.restype = i32
+        lib.ssd_scan_get_status.argtypes = [vp, vp]
+        lib.ssd_scan_get_status.restype = i32
+        lib.ssd_scan_strerror.argtypes = [i32]
+        lib.ssd_scan_strerror.restype = ctypes.c_char_p
+        lib.ssd_scan_version.argtypes = []
+        lib.ssd_scan_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return SSD_F32
+    if t == torch.bfloat16:
+        return SSD_BF16
+    raise TypeError(f"ssd_scan: unsupported element type {t} (float32 or bfloat16)")
+
+
+def make_dims(x: torch.Tensor, B: torch.Tensor) -> ssd_dims:
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    return ssd_dims(b, L, H, P, N, G, _dtype_code(x.dtype))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def ssd_scan_strerror(code: int) -> str:
+    return load_library().ssd_scan_strerror(int(code)).decode()
+
+
+def ssd_scan_version() -> int:
+    return load_library().ssd_scan_version()
+
+
+def ssd_scan_resolve_path(dims: ssd_dims, chunk_size: int, path: int = SSD_PATH_AUTO) -> int:
+    return load_library().ssd_scan_resolve_path(ctypes.byref(dims), int(chunk_size), int(path))
+
+
+def ssd_scan_workspace_bytes(dims: ssd_dims, chunk_size: int, path: int = SSD_PATH_AUTO) -> int:
+    return load_library().ssd_scan_workspace_bytes(ctypes.byref(dims), int(chunk_size), int(path))
+
+
+def _check_inputs(x, dt, A, B, C, D, initial_state):
+    if x.dim() != 4 or dt.dim() != 3 or B.dim() != 4 or C.dim() != 4:
+        raise ValueError("ssd_scan: x [b,L,H,P], dt [b,L,H], B/C [b,L,G,N] expected")
+    b, L, H, P = x.shape
+    if dt.shape != (b, L, H) or B.shape[:2] != (b, L) or C.shape != B.shape:
+        raise ValueError("ssd_scan: inconsistent shapes")
+    for name, t in (("dt", dt), ("B", B), ("C", C)):
+        if t.dtype != x.dtype:
+            raise TypeError(f"ssd_scan: {name} must have x's dtype {x.dtype}")
+    if A.shape != (H,) or A.dtype != torch.float32:
+        raise ValueError("ssd_scan: A must be float32 [H]")
+    if D is not None and (D.shape != (H,) or D.dtype != torch.float32):
+        raise ValueError("ssd_scan: D must be float32 [H]")
+    N = B.shape[3]
+    if initial_state is not None and (initial_state.shape != (b, H, P, N)
+                                      or initial_state.dtype != torch.float32):
+        raise ValueError("ssd_scan: initial_state must be float32 [b,H,P,N]")
+    for t in (x, dt, A, B, C, D, initial_state):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("ssd_scan: tensors must be contiguous")
+
+
+def ssd_scan_fwd(x, dt, A, B, C, D=None, initial_state=None, chunk_size: int = 256,
+                 path: int = SSD_PATH_AUTO, y=None, final_state=None, workspace=None,
+                 return_final_state: bool = True):
+    """y, final_state = scan(x, dt, A, B, C, D, initial_state) on x's CUDA device.
+
+    Enqueued on torch's current stream; outputs (and the workspace, unless given) are
+    allocated with torch.  Raises SSDError on any non-zero return code.
+    """
+    _check_inputs(x, dt, A, B, C, D, initial_state)
+    if not x.is_cuda:
+        raise ValueError("ssd_scan_fwd: tensors must be on a CUDA device (see ssd_scan_fwd_host)")
+    lib = load_library()
+    dims = make_dims(x, B)
+    b, L, H, P = x.shape
+    N = B.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
+    need = lib.ssd_scan_workspace_bytes(ctypes.byref(dims), int(chunk_size), int(path))
+    if need == 0:
+        rc = lib.ssd_scan_resolve_path(ctypes.byref(dims), int(chunk_size), int(path))
+        raise SSDError(-rc if rc < 0 else SSD_ERR_INVALID, "ssd_scan_workspace_bytes")
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    args = (ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+            _ptr(initial_state), int(chunk_size), _ptr(y), _ptr(final_state), _ptr(workspace),
+            workspace.numel(), _stream_handle(x.device))
+    if path == SSD_PATH_AUTO:
+        rc = lib.ssd_scan_fwd(*args)
+    else:
+        rc = lib.ssd_scan_fwd_path(*args, int(path))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_scan_fwd")
+    return y, final_state
+
+
+def ssd_scan_get_status(workspace, device=None) -> int:
+    """Synchronise the current stream and return (and clear) the workspace status word."""
+    lib = load_library()
+    return lib.ssd_scan_get_status(_ptr(workspace), _stream_handle(device or workspace.device))
+
+
+def ssd_scan_host_arena_bytes(dims: ssd_dims, chunk_size: int) -> int:
+    return load_library().ssd_scan_host_arena_bytes(ctypes.byref(dims), int(chunk_size))
+
+
+def ssd_scan_fwd_host(x, dt, A, B, C, D=None, initial_state=None, chunk_size: int = 256,
+                      y=None, final_state=None, arena=None, device=None):
+    """The host-buffer entry point: CPU tensors in and out (pinned memory recommended).
+
+    Copies in, scans and copies out on the current stream of ``device`` and synchronises it
+    before returning.  ``arena`` (a CUDA uint8 tensor) is reused when given and large enough.
+    """
+    _check_inputs(x, dt, A, B, C, D, initial_state)
+    if x.is_cuda:
+        raise ValueError("ssd_scan_fwd_host: tensors must be host tensors")
+    device = torch.device(device or "cuda")
+    lib = load_library()
+    dims = make_dims(x, B)
+    b, L, H, P = x.shape
+    N = B.shape[3]
+    if y is None:
+        y = torch.empty_like(x, pin_memory=True)
+    if final_state is None:
+        final_state = torch.empty((b, H, P, N), dtype=torch.float32, pin_memory=True)
+    need = lib.ssd_scan_host_arena_bytes(ctypes.byref(dims), int(chunk_size))
+    if need == 0:
+        raise SSDError(SSD_ERR_INVALID, "ssd_scan_host_arena_bytes")
+    if arena is None or arena.numel() < need:
+        arena = torch.empty(need, dtype=torch.uint8, device=device)
+    stream = _stream_handle(device)
+    rc = lib.ssd_scan_fwd_host(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                               _ptr(D), _ptr(initial_state), int(chunk_size), _ptr(y),
+                               _ptr(final_state), _ptr(arena), arena.numel(), stream)
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_scan_fwd_host")
+    torch.cuda.current_stream(device).synchronize()
+    return y, final_state

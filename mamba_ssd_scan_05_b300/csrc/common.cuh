@@ -1,0 +1,64 @@
+// common.cuh -- shared host/device definitions of libssd_scan (internal; not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ssd_scan.h"
+
+namespace ssd {
+
+// Workspace layout shared by all paths: the first 256 bytes hold the status word (int32 at
+// offset 0) and reserved space; path-specific regions follow at 256-byte aligned offsets.
+constexpr size_t kWsHeaderBytes = 256;
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Arguments of one scan, after validation, as the kernels see them.
+struct ScanArgs {
+    int64_t batch, seqlen, nheads, headdim, dstate, ngroups;
+    int32_t dtype;
+    int chunk;                 // Q
+    const void* x;
+    const void* dt;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;            // may be null
+    const float* h0;           // may be null
+    void* y;
+    float* hT;                 // may be null
+    uint8_t* ws;               // workspace base (256-byte aligned)
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);   // round to nearest even
+}
+
+// Records an error code in the status word (first writer wins).
+__device__ __forceinline__ void set_status(uint8_t* ws, int code) {
+    atomicCAS(reinterpret_cast<int*>(ws), 0, code);
+}
+
+// Chunked path (chunked.cu).
+size_t chunked_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t P, int64_t N, int Q);
+bool chunked_supports(int64_t P, int64_t N, int Q);
+int chunked_launch(const ScanArgs& a);
+
+// Tensor-core path (tc.cu).
+size_t tc_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t P, int64_t N, int Q);
+bool tc_supports(int32_t dtype, int64_t P, int64_t N, int Q);
+int tc_launch(const ScanArgs& a);
+
+}  // namespace ssd

@@ -1,0 +1,215 @@
+// ssd_scan.cu -- the C ABI of libssd_scan.so: argument checks, kernel-family dispatch, the
+// host-buffer variant and status reporting.  Every declaration is in include/ssd_scan.h.
+#include <string.h>
+
+#include "common.cuh"
+
+using namespace ssd;
+
+namespace {
+
+constexpr int kMaxChunk = 256;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t elem_bytes(int32_t dtype) { return dtype == SSD_F32 ? 4 : 2; }
+
+// Shape checks shared by every entry point.  Returns SSD_OK or SSD_ERR_INVALID.
+int check_dims(const ssd_dims* d, int chunk_size) {
+    if (!d) return SSD_ERR_INVALID;
+    if (d->batch < 1 || d->seqlen < 0 || d->nheads < 1 || d->headdim < 1 || d->dstate < 1 ||
+        d->ngroups < 1)
+        return SSD_ERR_INVALID;
+    if (d->nheads % d->ngroups != 0) return SSD_ERR_INVALID;
+    if (d->dtype != SSD_F32 && d->dtype != SSD_BF16) return SSD_ERR_INVALID;
+    if (chunk_size < 1 || chunk_size > kMaxChunk) return SSD_ERR_INVALID;
+    // keep every element count comfortably inside int64 arithmetic
+    const double elems = (double)d->batch * (double)d->seqlen * (double)d->nheads *
+                         (double)d->headdim;
+    const double states = (double)d->batch * (double)d->nheads * (double)d->headdim *
+                          (double)d->dstate;
+    if (elems > 4.0e15 || states > 4.0e15) return SSD_ERR_INVALID;
+    return SSD_OK;
+}
+
+int resolve(const ssd_dims* d, int chunk_size, int path) {
+    const int rc = check_dims(d, chunk_size);
+    if (rc != SSD_OK) return -rc;
+    const bool tc_ok = tc_supports(d->dtype, d->headdim, d->dstate, chunk_size);
+    const bool ch_ok = chunked_supports(d->headdim, d->dstate, chunk_size);
+    switch (path) {
+        case SSD_PATH_AUTO:
+            if (tc_ok) return SSD_PATH_TC;
+            if (ch_ok) return SSD_PATH_CHUNKED;
+            return -SSD_ERR_UNSUPPORTED;
+        case SSD_PATH_TC: return tc_ok ? SSD_PATH_TC : -SSD_ERR_UNSUPPORTED;
+        case SSD_PATH_CHUNKED: return ch_ok ? SSD_PATH_CHUNKED : -SSD_ERR_UNSUPPORTED;
+        default: return -SSD_ERR_INVALID;
+    }
+}
+
+size_t workspace_for(const ssd_dims* d, int chunk_size, int resolved) {
+    if (resolved == SSD_PATH_TC)
+        return tc_workspace_bytes(d->batch, d->seqlen, d->nheads, d->headdim, d->dstate,
+                                  chunk_size);
+    return chunked_workspace_bytes(d->batch, d->seqlen, d->nheads, d->headdim, d->dstate,
+                                   chunk_size);
+}
+
+int run(const ssd_dims* d, const void* x, const void* dt, const float* A, const void* B,
+        const void* C, const float* D, const float* h0, int chunk_size, void* y, float* hT,
+        void* workspace, size_t workspace_bytes, void* stream, int path) {
+    const int r = resolve(d, chunk_size, path);
+    if (r < 0) return -r;
+    if (!A || (d->seqlen > 0 && (!x || !dt || !B || !C || !y))) return SSD_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(B, 16) || !aligned(C, 16) ||
+        !aligned(y, 16) || !aligned(A, 4) || !aligned(D, 4) || !aligned(h0, 4) ||
+        !aligned(hT, 4))
+        return SSD_ERR_INVALID;
+    if (!workspace || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
+    if (workspace_bytes < workspace_for(d, chunk_size, r)) return SSD_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the status word reports on this call only
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
+    if (d->seqlen == 0) {
+        if (!hT) return SSD_OK;
+        const size_t sb = sizeof(float) * (size_t)(d->batch * d->nheads * d->headdim * d->dstate);
+        const cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, sb, cudaMemcpyDeviceToDevice, st)
+                                 : cudaMemsetAsync(hT, 0, sb, st);
+        return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    }
+    ScanArgs a;
+    a.batch = d->batch; a.seqlen = d->seqlen; a.nheads = d->nheads; a.headdim = d->headdim;
+    a.dstate = d->dstate; a.ngroups = d->ngroups; a.dtype = d->dtype; a.chunk = chunk_size;
+    a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.h0 = h0; a.y = y; a.hT = hT;
+    a.ws = static_cast<uint8_t*>(workspace); a.ws_bytes = workspace_bytes; a.stream = st;
+    return r == SSD_PATH_TC ? tc_launch(a) : chunked_launch(a);
+}
+
+// Byte sizes of every tensor of a problem, in the host-arena order.
+struct Sizes {
+    size_t x, dt, A, bc, D, st;
+};
+Sizes sizes_of(const ssd_dims* d) {
+    Sizes s;
+    const size_t eb = elem_bytes(d->dtype);
+    s.x = eb * (size_t)(d->batch * d->seqlen * d->nheads * d->headdim);
+    s.dt = eb * (size_t)(d->batch * d->seqlen * d->nheads);
+    s.A = sizeof(float) * (size_t)d->nheads;
+    s.bc = eb * (size_t)(d->batch * d->seqlen * d->ngroups * d->dstate);
+    s.D = sizeof(float) * (size_t)d->nheads;
+    s.st = sizeof(float) * (size_t)(d->batch * d->nheads * d->headdim * d->dstate);
+    return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssd_scan_resolve_path(const ssd_dims* dims, int chunk_size, int path) {
+    return resolve(dims, chunk_size, path);
+}
+
+size_t ssd_scan_workspace_bytes(const ssd_dims* dims, int chunk_size, int path) {
+    const int r = resolve(dims, chunk_size, path);
+    if (r < 0) return 0;
+    return workspace_for(dims, chunk_size, r);
+}
+
+int ssd_scan_fwd(const ssd_dims* dims, const void* x, const void* dt, const float* A,
+                 const void* B, const void* C, const float* D, const float* initial_state,
+                 int chunk_size, void* y, float* final_state, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+    return run(dims, x, dt, A, B, C, D, initial_state, chunk_size, y, final_state, workspace,
+               workspace_bytes, stream, SSD_PATH_AUTO);
+}
+
+int ssd_scan_fwd_path(const ssd_dims* dims, const void* x, const void* dt, const float* A,
+                      const void* B, const void* C, const float* D, const float* initial_state,
+                      int chunk_size, void* y, float* final_state, void* workspace,
+                      size_t workspace_bytes, void* stream, int path) {
+    if (path == SSD_PATH_AUTO) return SSD_ERR_INVALID;
+    return run(dims, x, dt, A, B, C, D, initial_state, chunk_size, y, final_state, workspace,
+               workspace_bytes, stream, path);
+}
+
+size_t ssd_scan_host_arena_bytes(const ssd_dims* dims, int chunk_size) {
+    const int r = resolve(dims, chunk_size, SSD_PATH_AUTO);
+    if (r < 0) return 0;
+    const Sizes s = sizes_of(dims);
+    return align_up(s.x, 256) * 2 + align_up(s.dt, 256) + align_up(s.A, 256) +
+           align_up(s.bc, 256) * 2 + align_up(s.D, 256) + align_up(s.st, 256) * 2 +
+           workspace_for(dims, chunk_size, r);
+}
+
+int ssd_scan_fwd_host(const ssd_dims* dims, const void* x, const void* dt, const float* A,
+                      const void* B, const void* C, const float* D, const float* initial_state,
+                      int chunk_size, void* y, float* final_state, void* device_arena,
+                      size_t arena_bytes, void* stream) {
+    const int r = resolve(dims, chunk_size, SSD_PATH_AUTO);
+    if (r < 0) return -r;
+    if (!A || (dims->seqlen > 0 && (!x || !dt || !B || !C || !y))) return SSD_ERR_INVALID;
+    if (!device_arena || !aligned(device_arena, 256)) return SSD_ERR_INVALID;
+    if (arena_bytes < ssd_scan_host_arena_bytes(dims, chunk_size)) return SSD_ERR_WORKSPACE;
+    const Sizes s = sizes_of(dims);
+    uint8_t* p = static_cast<uint8_t*>(device_arena);
+    auto take = [&p](size_t n) { uint8_t* q = p; p += align_up(n, 256); return q; };
+    uint8_t* dx = take(s.x);
+    uint8_t* ddt = take(s.dt);
+    float* dA = reinterpret_cast<float*>(take(s.A));
+    uint8_t* dB = take(s.bc);
+    uint8_t* dC = take(s.bc);
+    float* dD = reinterpret_cast<float*>(take(s.D));
+    float* dh0 = reinterpret_cast<float*>(take(s.st));
+    uint8_t* dy = take(s.x);
+    float* dhT = reinterpret_cast<float*>(take(s.st));
+    uint8_t* dws = p;
+    const size_t ws_bytes = arena_bytes - (size_t)(p - static_cast<uint8_t*>(device_arena));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    if ((s.x && cudaMemcpyAsync(dx, x, s.x, h2d, st) != cudaSuccess) ||
+        (s.dt && cudaMemcpyAsync(ddt, dt, s.dt, h2d, st) != cudaSuccess) ||
+        cudaMemcpyAsync(dA, A, s.A, h2d, st) != cudaSuccess ||
+        (s.bc && cudaMemcpyAsync(dB, B, s.bc, h2d, st) != cudaSuccess) ||
+        (s.bc && cudaMemcpyAsync(dC, C, s.bc, h2d, st) != cudaSuccess) ||
+        (D && cudaMemcpyAsync(dD, D, s.D, h2d, st) != cudaSuccess) ||
+        (initial_state && cudaMemcpyAsync(dh0, initial_state, s.st, h2d, st) != cudaSuccess))
+        return SSD_ERR_CUDA;
+    const int rc = run(dims, dx, ddt, dA, dB, dC, D ? dD : nullptr,
+                       initial_state ? dh0 : nullptr, chunk_size, dy,
+                       final_state ? dhT : nullptr, dws, ws_bytes, stream, SSD_PATH_AUTO);
+    if (rc != SSD_OK) return rc;
+    if ((s.x && cudaMemcpyAsync(y, dy, s.x, d2h, st) != cudaSuccess) ||
+        (final_state && cudaMemcpyAsync(final_state, dhT, s.st, d2h, st) != cudaSuccess))
+        return SSD_ERR_CUDA;
+    return SSD_OK;
+}
+
+int ssd_scan_get_status(void* workspace, void* stream) {
+    if (!workspace) return SSD_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    return v == 0 ? SSD_OK : v;
+}
+
+const char* ssd_scan_strerror(int code) {
+    switch (code) {
+        case SSD_OK: return "ok";
+        case SSD_ERR_INVALID: return "invalid argument (pointer, alignment, size or shape)";
+        case SSD_ERR_UNSUPPORTED: return "problem not supported by the selected kernel family";
+        case SSD_ERR_CUDA: return "CUDA runtime error";
+        case SSD_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+        case SSD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        default: return "unknown error code";
+    }
+}
+
+int ssd_scan_version(void) { return 100; }
+
+}  // extern "C"

@@ -88,11 +88,11 @@ int ssd_oracle_scan(int64_t n_problems, int64_t L, int64_t P, int64_t N,
     int used = 1;
     int failed = 0;
 #ifdef _OPENMP
-    if (n_threads > 0) omp_set_num_threads(n_threads);
+    const int nt = n_threads > 0 ? n_threads : omp_get_max_threads();
 #else
     (void)n_threads;
 #endif
-#pragma omp parallel reduction(max : used) reduction(| : failed)
+#pragma omp parallel num_threads(nt) reduction(max : used) reduction(| : failed)
     {
 #ifdef _OPENMP
         used = omp_get_num_threads();

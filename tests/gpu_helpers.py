@@ -1,0 +1,78 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI, compare to the oracle."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import torch
+
+import oracle
+from mamba_ssd_scan_05_b300 import workloads
+
+# Tolerances: max|dy| / max|y_ref| and sum|dy| / sum|y_ref| (float32 storage: 1e-4 on the max;
+# bf16 storage with float32 accumulation: 2e-2 on the max, 5e-3 on the mean); final_state to
+# the same bounds.
+TOL = {"f32": (1e-4, 1e-4), "bf16": (2e-2, 5e-3)}
+
+
+def dtype_name(t: torch.dtype) -> str:
+    return "f32" if t == torch.float32 else "bf16"
+
+
+def to_device(inp: dict, device="cuda") -> dict:
+    return {k: (None if v is None else v.to(device, non_blocking=False).contiguous())
+            for k, v in inp.items()}
+
+
+def run_gpu(inp_dev: dict, chunk: int, path: int = -1, use_D: bool = True, use_h0: bool = True):
+    from mamba_ssd_scan_05_b300 import ssd_scan_fwd, ssd_scan_get_status
+    ws_holder = {}
+    y, hT = ssd_scan_fwd(inp_dev["x"], inp_dev["dt"], inp_dev["A"], inp_dev["B"], inp_dev["C"],
+                         inp_dev["D"] if use_D else None,
+                         inp_dev["h0"] if use_h0 else None, chunk_size=chunk, path=path)
+    torch.cuda.synchronize()
+    return y, hT
+
+
+def assert_close(got, ref, dtype: str, what: str):
+    mx, mean = oracle.error_metrics(got, ref)
+    tmax, tmean = TOL[dtype]
+    assert np.all(np.isfinite(oracle._f64(got))), f"{what}: non-finite values"
+    assert mx <= tmax, f"{what}: max rel err {mx:.3e} > {tmax:.0e}"
+    assert mean <= tmean, f"{what}: mean rel err {mean:.3e} > {tmean:.0e}"
+    return mx, mean
+
+
+def check_against_oracle(inp_cpu: dict, y_dev, hT_dev, heads=None, use_D=True, use_h0=True,
+                         what=""):
+    """Compare GPU outputs with the oracle on all heads, or on the sampled (b, h) heads."""
+    dt_name = dtype_name(inp_cpu["x"].dtype)
+    D = inp_cpu["D"] if use_D else None
+    h0 = inp_cpu["h0"] if use_h0 else None
+    if heads is None:
+        y_ref, h_ref = oracle.scan(inp_cpu["x"], inp_cpu["dt"], inp_cpu["A"], inp_cpu["B"],
+                                   inp_cpu["C"], D, h0)
+        got_y = y_dev.float().cpu()
+        got_h = None if hT_dev is None else hT_dev.cpu()
+    else:
+        y_ref, h_ref = oracle.scan(inp_cpu["x"], inp_cpu["dt"], inp_cpu["A"], inp_cpu["B"],
+                                   inp_cpu["C"], D, h0, heads=heads)
+        got_y = torch.stack([y_dev[b, :, h, :].float().cpu() for b, h in heads])
+        got_h = None if hT_dev is None else torch.stack([hT_dev[b, h].cpu() for b, h in heads])
+    r = {"y": assert_close(got_y, y_ref, dt_name, f"{what} y")}
+    if got_h is not None:
+        r["final_state"] = assert_close(got_h, h_ref, dt_name, f"{what} final_state")
+    return r
+
+
+@functools.lru_cache(maxsize=2)
+def workload_inputs(idx: int) -> dict:
+    return workloads.make_inputs(workloads.WORKLOADS[idx])
+
+
+def sample_heads(b: int, H: int, k: int = 4, seed: int = 0):
+    rng = np.random.default_rng(seed)
+    heads = {(0, 0), (b - 1, H - 1)}
+    while len(heads) < min(k, b * H):
+        heads.add((int(rng.integers(b)), int(rng.integers(H))))
+    return sorted(heads)

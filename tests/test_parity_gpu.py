@@ -1,0 +1,183 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, element by element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import (TOL, assert_close, check_against_oracle, run_gpu, sample_heads,
+                         to_device, workload_inputs)
+from mamba_ssd_scan_05_b300 import (SSD_PATH_AUTO, SSD_PATH_CHUNKED, SSD_PATH_TC, SSDError,
+                                    make_dims, ssd_scan_fwd, ssd_scan_fwd_host,
+                                    ssd_scan_get_status, ssd_scan_resolve_path, workloads)
+
+pytestmark = pytest.mark.gpu
+
+
+def available_paths(inp, chunk):
+    dims = make_dims(inp["x"], inp["B"])
+    return [p for p in (SSD_PATH_CHUNKED, SSD_PATH_TC) if ssd_scan_resolve_path(dims, chunk, p) == p]
+
+
+# ---- the five workloads at full size (sampled heads for the large ones) --------------------
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
+def test_workload_full_size(idx):
+    w = workloads.WORKLOADS[idx]
+    inp = workload_inputs(idx)
+    dev = to_device(inp)
+    y, hT = run_gpu(dev, w.chunk)
+    heads = None if idx == 0 else sample_heads(w.batch, w.nheads, k=4, seed=idx)
+    check_against_oracle(inp, y, hT, heads=heads, what=w.name)
+    assert ssd_scan_get_status(torch.empty(256, dtype=torch.uint8, device="cuda")) == 0
+
+
+# ---- small cases: several tiles, ragged tails, every kernel family that takes the shape ----
+
+SMALL = [
+    # b, L, H, P, N, G, Q, dtype, h0
+    (2, 300, 4, 64, 128, 1, 256, "bf16", False),
+    (1, 1000, 8, 64, 128, 2, 128, "bf16", True),
+    (2, 520, 4, 128, 256, 2, 128, "bf16", True),
+    (1, 384, 2, 64, 128, 1, 64, "bf16", True),
+    (1, 333, 3, 40, 24, 1, 64, "bf16", False),
+    (2, 200, 4, 32, 16, 1, 64, "f32", False),
+    (1, 257, 2, 16, 16, 1, 7, "f32", True),
+    (1, 130, 2, 8, 8, 2 // 2, 1, "f32", True),
+    (1, 129, 4, 64, 256, 4, 256, "f32", True),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "b{}L{}H{}P{}N{}G{}Q{}{}{}".format(
+    *c[:8], "h0" if c[8] else ""))
+def test_small_cases_all_paths(case):
+    b, L, H, P, N, G, Q, dt, with_h0 = case
+    inp = workloads.make_shape_inputs(b, L, H, P, N, G, dt, seed=L + P,
+                                      h0_mode="normal" if with_h0 else "none", d_mode="normal")
+    dev = to_device(inp)
+    paths = available_paths(inp, Q)
+    assert paths, "no kernel family takes this shape"
+    for path in paths:
+        y, hT = run_gpu(dev, Q, path=path)
+        check_against_oracle(inp, y, hT, what=f"path{path}")
+
+
+# ---- edge cases -------------------------------------------------------------------------
+
+def test_empty_sequence_returns_initial_state():
+    inp = workloads.make_shape_inputs(2, 0, 4, 64, 128, 1, "bf16", seed=1, h0_mode="normal")
+    dev = to_device(inp)
+    y, hT = run_gpu(dev, 256)
+    assert y.numel() == 0
+    assert torch.equal(hT.cpu(), inp["h0"])
+    y, hT = run_gpu(dev, 256, use_h0=False)
+    assert torch.count_nonzero(hT) == 0
+
+
+@pytest.mark.parametrize("L", [1, 2, 127, 128, 129])
+def test_short_sequences(L):
+    inp = workloads.make_shape_inputs(1, L, 4, 64, 128, 1, "bf16", seed=L, h0_mode="normal")
+    dev = to_device(inp)
+    for path in available_paths(inp, 256):
+        y, hT = run_gpu(dev, 256, path=path)
+        check_against_oracle(inp, y, hT, what=f"L={L} path{path}")
+
+
+def test_no_skip_no_initial_state_no_final():
+    inp = workloads.make_shape_inputs(1, 300, 4, 64, 128, 1, "bf16", seed=5)
+    dev = to_device(inp)
+    y, hT = ssd_scan_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], None, None,
+                         chunk_size=256, return_final_state=False)
+    torch.cuda.synchronize()
+    assert hT is None
+    check_against_oracle(inp, y, None, use_D=False, use_h0=False, what="no D")
+
+
+@pytest.mark.parametrize("Q", [32, 64, 128, 256])
+def test_chunk_size_invariance(Q):
+    inp = workloads.make_shape_inputs(1, 1024, 4, 64, 128, 1, "bf16", seed=9, h0_mode="normal")
+    dev = to_device(inp)
+    for path in available_paths(inp, Q):
+        y, hT = run_gpu(dev, Q, path=path)
+        check_against_oracle(inp, y, hT, what=f"Q={Q} path{path}")
+
+
+def test_both_families_agree_bf16():
+    inp = workloads.make_shape_inputs(2, 640, 4, 64, 128, 1, "bf16", seed=3, h0_mode="normal")
+    dev = to_device(inp)
+    paths = available_paths(inp, 256)
+    outs = [run_gpu(dev, 256, path=p) for p in paths]
+    for y, hT in outs[1:]:
+        assert_close(y.float().cpu(), outs[0][0].float().cpu(), "bf16", "families y")
+        assert_close(hT.cpu(), outs[0][1].cpu(), "bf16", "families final")
+
+
+# ---- closed forms on the GPU --------------------------------------------------------------
+
+def test_gpu_a_zero_is_running_sum():
+    inp = workloads.make_shape_inputs(1, 700, 2, 64, 128, 1, "bf16", seed=2)
+    inp["A"] = torch.zeros_like(inp["A"])
+    inp["B"] = torch.zeros_like(inp["B"])
+    inp["C"] = torch.zeros_like(inp["C"])
+    inp["B"][..., 0] = 1.0
+    inp["C"][..., 0] = 1.0
+    dev = to_device(inp)
+    x = inp["x"].double().numpy()
+    dt = inp["dt"].double().numpy()
+    ref = np.cumsum(dt[..., None] * x, axis=1) + inp["D"].double().numpy()[None, None, :, None] * x
+    for path in available_paths(inp, 256):
+        y, _ = run_gpu(dev, 256, path=path)
+        assert_close(y.float().cpu(), ref, "bf16", f"A=0 path{path}")
+
+
+def test_gpu_dt_zero_tokens_freeze_state():
+    inp = workloads.make_shape_inputs(1, 512, 4, 64, 128, 1, "bf16", seed=4, h0_mode="normal")
+    inp["dt"][:, 200:512] = 0.0
+    dev = to_device(inp)
+    short = {k: (v[:, :200].contiguous() if k in ("x", "dt", "B", "C") else v)
+             for k, v in dev.items()}
+    for path in available_paths(inp, 128):
+        _, h_full = run_gpu(dev, 128, path=path)
+        _, h_200 = run_gpu(short, 128, path=path)
+        assert torch.allclose(h_full, h_200, rtol=1e-5, atol=1e-6)
+
+
+def test_gpu_sequence_split_matches_one_call():
+    """Running [0, L1) then [L1, L) with initial_state = final_state equals one call."""
+    w = workloads.WORKLOADS[2]
+    inp = workload_inputs(2)
+    dev = to_device(inp)
+    L1 = 1536 + 40
+    first = {k: (v[:, :L1].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in dev.items()}
+    second = {k: (v[:, L1:].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in dev.items()}
+    y, hT = run_gpu(dev, w.chunk)
+    y1, h1 = run_gpu(first, w.chunk)
+    second["h0"] = h1
+    y2, h2 = run_gpu(second, w.chunk)
+    assert_close(torch.cat([y1, y2], dim=1).float().cpu(), y.float().cpu(), "bf16", "split y")
+    assert_close(h2.cpu(), hT.cpu(), "bf16", "split final")
+
+
+# ---- API behaviour on the device -----------------------------------------------------------
+
+def test_host_entry_point_matches_device_entry_point():
+    inp = workloads.make_shape_inputs(2, 400, 4, 64, 128, 2, "bf16", seed=6, h0_mode="normal")
+    pinned = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+    y_h, h_h = ssd_scan_fwd_host(pinned["x"], pinned["dt"], pinned["A"], pinned["B"],
+                                 pinned["C"], pinned["D"], pinned["h0"], chunk_size=128)
+    dev = to_device(inp)
+    y_d, h_d = run_gpu(dev, 128)
+    assert torch.equal(y_h, y_d.cpu())
+    assert torch.equal(h_h, h_d.cpu())
+
+
+def test_device_errors_raise():
+    inp = workloads.make_shape_inputs(1, 64, 4, 64, 128, 1, "bf16", seed=7)
+    dev = to_device(inp)
+    with pytest.raises(SSDError):
+        ssd_scan_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], chunk_size=0)
+    tiny_ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(SSDError):
+        ssd_scan_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], chunk_size=64,
+                     workspace=tiny_ws[:16])
+    with pytest.raises(TypeError):
+        ssd_scan_fwd(dev["x"].float(), dev["dt"], dev["A"], dev["B"], dev["C"])
