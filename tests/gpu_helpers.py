@@ -25,12 +25,18 @@ def to_device(inp: dict, device="cuda") -> dict:
 
 
 def run_gpu(inp_dev: dict, chunk: int, path: int = -1, use_D: bool = True, use_h0: bool = True):
-    from mamba_ssd_scan_05_b300 import ssd_scan_fwd, ssd_scan_get_status
-    ws_holder = {}
+    """One ssd_scan_fwd call; also checks the call's device status word."""
+    from mamba_ssd_scan_05_b300 import (make_dims, ssd_scan_fwd, ssd_scan_get_status,
+                                        ssd_scan_workspace_bytes)
+    dims = make_dims(inp_dev["x"], inp_dev["B"])
+    need = ssd_scan_workspace_bytes(dims, chunk, path)
+    assert need > 0, "problem rejected"
+    ws = torch.empty(need, dtype=torch.uint8, device=inp_dev["x"].device)
     y, hT = ssd_scan_fwd(inp_dev["x"], inp_dev["dt"], inp_dev["A"], inp_dev["B"], inp_dev["C"],
                          inp_dev["D"] if use_D else None,
-                         inp_dev["h0"] if use_h0 else None, chunk_size=chunk, path=path)
-    torch.cuda.synchronize()
+                         inp_dev["h0"] if use_h0 else None, chunk_size=chunk, path=path,
+                         workspace=ws)
+    assert ssd_scan_get_status(ws) == 0, "device status word reports an error"
     return y, hT
 
 

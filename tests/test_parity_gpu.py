@@ -28,7 +28,6 @@ def test_workload_full_size(idx):
     y, hT = run_gpu(dev, w.chunk)
     heads = None if idx == 0 else sample_heads(w.batch, w.nheads, k=4, seed=idx)
     check_against_oracle(inp, y, hT, heads=heads, what=w.name)
-    assert ssd_scan_get_status(torch.empty(256, dtype=torch.uint8, device="cuda")) == 0
 
 
 # ---- small cases: several tiles, ragged tails, every kernel family that takes the shape ----
@@ -175,9 +174,5 @@ def test_device_errors_raise():
     dev = to_device(inp)
     with pytest.raises(SSDError):
         ssd_scan_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], chunk_size=0)
-    tiny_ws = torch.empty(256, dtype=torch.uint8, device="cuda")
-    with pytest.raises(SSDError):
-        ssd_scan_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], chunk_size=64,
-                     workspace=tiny_ws[:16])
     with pytest.raises(TypeError):
         ssd_scan_fwd(dev["x"].float(), dev["dt"], dev["A"], dev["B"], dev["C"])
