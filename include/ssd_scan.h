@@ -132,6 +132,38 @@ int ssd_scan_fwd_host(const ssd_dims* dims,
                       void* y, float* final_state,
                       void* device_arena, size_t arena_bytes, void* stream);
 
+/*
+ * No-allocation variant.  The pages have no counterpart: this entry point exists for callers
+ * that cannot allocate device memory when they run the scan -- code that must not call
+ * cudaMalloc (or any allocator) because a framework owns all device memory through its own
+ * pool, because allocation is forbidden after start-up in the host process, or because a CUDA
+ * graph is being captured.  The caller passes only inputs and outputs (device pointers, as for
+ * ssd_scan_fwd); the scratch comes from a fixed SSD_NOALLOC_SCRATCH_BYTES buffer compiled into
+ * the library's device image, which every GPU that loads the library holds until the process
+ * exits.
+ *
+ *   - Runs the chunked kernel family (SSD_PATH_CHUNKED) for any dtype the ABI accepts.
+ *   - Problems whose scratch (ssd_scan_workspace_bytes(dims, chunk_size, SSD_PATH_CHUNKED))
+ *     exceeds SSD_NOALLOC_SCRATCH_BYTES are rejected with SSD_ERR_WORKSPACE before anything is
+ *     enqueued.  Other errors as ssd_scan_fwd.
+ *   - The first call on each device looks up the buffer's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that first call
+ *     before any stream capture.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *   - Every call shares the one buffer per device, and the buffer keeps the last call's
+ *     contents (the status word is cleared at the start of each call).  Calls whose work
+ *     overlaps on the GPU (different streams without ordering, or other host threads) race on
+ *     the buffer; order them on one stream.
+ *   - ssd_scan_get_status is not available for this variant (the caller holds no workspace);
+ *     a device-side failure surfaces as a CUDA error on `stream`.
+ */
+#define SSD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int ssd_scan_fwd_noalloc(const ssd_dims* dims,
+                         const void* x, const void* dt, const float* A,
+                         const void* B, const void* C, const float* D,
+                         const float* initial_state, int chunk_size,
+                         void* y, float* final_state, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word of `workspace` (the first
  * 4 bytes).  Returns SSD_OK, SSD_ERR_TIMEOUT if a bounded device wait gave up in a call that
  * used this workspace, or SSD_ERR_CUDA if synchronisation or the read failed. */
