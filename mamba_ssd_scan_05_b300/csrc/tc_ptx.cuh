@@ -179,12 +179,33 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         : "memory");
 }
 
+// ---- global flags (cross-CTA hand-off) ------------------------------------------------------
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* a) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* a, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(int* a, int v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
 // ---- small numeric helpers -----------------------------------------------------------------
 
 // 2^x with the hardware approximation (ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log2(x) with the hardware approximation (lg2.approx, flush-to-zero; log2(0) = -inf).
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
