@@ -6,8 +6,8 @@
 //
 //   S1  cum_i = sum_{k<=i} dt_k A  (inside the tile); L_ij = exp(cum_i - cum_j) for i >= j
 //   S2  G = C B^T                         tcgen05.mma  M=128 N=128 K=d_state   (TMEM)
-//       P = L o G o dt_j  -> bf16 (smem)  CUDA cores (mask first, then exp)
-//       Y_diag = P X                      tcgen05.mma  M=128 N=64  K=128
+//       P = L o G o dt_j  -> bf16, written back into G's TMEM columns (CUDA cores, mask first)
+//       Y_diag = P X                      tcgen05.mma  A = P from TMEM, M=128 N=64 K=128
 //       S^T = B^T (diag(exp(cum_last - cum) dt) X)   M=d_state N=64 K=128
 //   S3  H = exp(cum_last) H + S^T         CUDA cores, H (= h^T, fp32) lives in TMEM
 //   S4  Y_off = C h_prev^T                tcgen05.mma  M=128 N=64  K=d_state
@@ -25,12 +25,15 @@
 // predecessor range ends with through a decoupled look-back over per-CTA slots in the
 // workspace (inclusive states, or aggregates (decay, local state) of range pieces).
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: x / B / C tiles of 128 tokens into a ring of smem stages
+// Warp roles (352 threads):
+//   warp 0      TMA producer of the B / C ring (2 stages for d_state 128)
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
-//   warps 2-5   "A" warpgroup: cumsum of dt*A, scaled copy of x for the state GEMM, P = L o G
-//   warps 6-9   "B" warpgroup: state recurrence in TMEM, bf16 h^T for the next tile, y epilogue,
-//               state hand-off between CTAs
+//   warp 2      producer of the x / decay ring: TMA of the x tile, and from dt (loaded two tiles
+//               ahead) the tile's log2-domain cumsum and every exponential factor the other
+//               roles need (3 stages)
+//   warps 3-6   "A" warpgroup: scaled copy of x for the state GEMM, half of P = L o G
+//   warps 7-10  "B" warpgroup: the other half of P, state recurrence, bf16 h^T for the next
+//               tile's off-diagonal GEMM, y epilogue, state hand-off between CTAs
 // Every wait is bounded (clock64 budget); a timeout sets SSD_ERR_TIMEOUT in the workspace
 // status word, makes every role stop, drains in-flight copies and frees TMEM before exit.
 #include <cuda.h>
@@ -48,27 +51,41 @@ using namespace ptx;
 
 constexpr int kTile = 128;          // tokens per tile (MMA M)
 constexpr int kPS = 64;             // headdim columns per unit (MMA N of Y, Y_off, S)
-constexpr int kThreads = 320;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDt = 2, kWarpA = 3, kWarpB = 7;
+constexpr int kThreads = 11 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTileBytes = kTile * 128;   // a 128-row x 128-byte swizzled tile (16 KB)
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpB = 6;   // warps 2-5: the A warpgroup
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxCtas = 256;       // grid cap (and number of hand-off slots in the workspace)
+constexpr int kXStagesMax = 3;      // x / decay ring depth (at most)
+
+// Per-tile decay factors (log2 domain: cum2 = cum * log2(e)), written by the decay producer.
+struct DtSlot {
+    float cum2[kTile];      // inclusive cumsum of dt * A * log2(e) inside the tile
+    float pcol[kTile];      // cum2 - log2(dt) (+inf where dt = 0): column term of L o dt
+    float w[kTile];         // exp2(cum2_last - cum2) * dt: decay to the tile end, times dt
+    float e[kTile];         // exp2(cum2): decay from the tile start (off-diagonal rows)
+    float urow[kTile];      // exp2(cum2 - m_q), m_q = cum2[32 q - 1], q = row / 32 >= 1
+    float colf[3][kTile];   // exp2(m_q - pcol), q = 1..3 (used for columns j < 32 q)
+    float clast2;           // cum2[kTile - 1]
+    float pad[3];
+};
 
 template <int NS>
 struct Cfg {
     static constexpr int kNReg = NS / 64;             // 64-column regions of a B / C tile
-    static constexpr int kStages = NS == 128 ? 2 : 1;
-    static constexpr int kGBuf = NS == 128 ? 2 : 1;
+    static constexpr int kXSt = NS == 128 ? 3 : 2;    // x / decay ring depth
+    static constexpr int kBCStages = NS == 128 ? 2 : 1;
+    static constexpr int kGBuf = NS == 128 ? 2 : 1;   // G / P buffers in TMEM
     static constexpr int kMB = NS / 128;               // 128-row blocks of the state
+    static constexpr uint32_t kBCBytes = 2 * kNReg * kTileBytes;
     // shared memory (byte offsets from a 1024-aligned base)
     static constexpr uint32_t kOffX = 0;
-    static constexpr uint32_t kOffB = kOffX + kStages * kTileBytes;
-    static constexpr uint32_t kOffC = kOffB + kStages * kNReg * kTileBytes;
-    static constexpr uint32_t kOffXt = kOffC + kStages * kNReg * kTileBytes;
-    static constexpr uint32_t kOffP = kOffXt + kTileBytes;
-    static constexpr uint32_t kOffHt = kOffP + 2 * kTileBytes;
-    static constexpr uint32_t kOffSmall = kOffHt + NS * 128;
+    static constexpr uint32_t kOffBC = kOffX + kXSt * kTileBytes;
+    static constexpr uint32_t kOffXt = kOffBC + kBCStages * kBCBytes;
+    static constexpr uint32_t kOffHt = kOffXt + kTileBytes;
+    static constexpr uint32_t kOffDt = kOffHt + NS * 128;
+    static constexpr uint32_t kOffSmall = kOffDt + kXSt * sizeof(DtSlot);
     // TMEM columns
     static constexpr uint32_t kColG = 0;
     static constexpr uint32_t kColY = kGBuf * 128;
@@ -76,20 +93,31 @@ struct Cfg {
     static constexpr uint32_t kColS = kColYoff + kPS;
     static constexpr uint32_t kColH = kColS + kMB * kPS;
     static_assert(kColH + kMB * kPS <= kTmemCols, "TMEM budget");
-    static constexpr uint32_t kStageTx = kTileBytes * (1 + 2 * kNReg);
+    static_assert(kXSt <= kXStagesMax, "x ring");
 };
 
-struct Small {
-    uint64_t full[2], empty[2], g_full[2], g_empty[2];
-    uint64_t xt_full, xt_empty, p_full, p_empty, s_full, s_empty, h_full, h_empty;
-    uint64_t y_full, y_empty, a_sync, b_sync, mma_done;
-    uint32_t tmem_base;
-    int abort_flag;
-    float a_cp[kTile];       // cum * log2(e) - log2(dt) per row ("A" warpgroup; +inf if dt = 0)
-    float a_wsum[2][4];      // per-warp scan totals, double-buffered by tile parity
-    float b_wsum[2][4];
-    int lb_kind;             // look-back step decided by one "B" thread: 1 inclusive, 2 aggregate
-    float lb_logd;           // that step's aggregate log2 decay
+enum : int { kInitH0 = 0, kInitZero = 1, kInitLookback = 2 };
+enum : int { kFinNone = 0, kFinFinal = 1, kFinIncl = 2, kFinAgg = 3 };
+
+struct Item {
+    int64_t u;        // unit
+    int k0, k1;       // tile range of the unit's chain
+    int pass1;        // 1: state-only pass (no y)
+    int init;         // how the state starts: kInit*
+    int fin;          // what happens to the state at the end: kFin*
+};
+
+// A CTA's range, as scalars (no arrays, so nothing of it lives in local memory).
+//
+// A range holds at most a tail piece of one chain (it needs the state the previous range
+// ends with), whole chains, and a head piece of another chain (its end state is needed by the
+// next range); or a middle piece of one chain.  Items run in this order: [state-only pass over
+// the piece with a successor, in pass1 mode], [head piece], [whole chains], [tail piece], so
+// the state a successor needs is published as early as possible and the state a range needs
+// is consumed as late as possible.
+struct Plan {
+    int64_t u0, u1, f_lo, n_full, n_items;
+    int k0, k1, n_pre, middle, p1;
 };
 
 struct TcParams {
@@ -106,123 +134,70 @@ struct TcParams {
     __nv_bfloat16* y;
     float* hT;
     uint8_t* ws;
-    int* flags;         // per CTA: [0] inclusive-state flag, [1] aggregate flag, [2] log2 decay
+    int* flags;         // per CTA and "B" warp: inclusive flag, aggregate flag, log2 decay
     float* slots;       // per CTA: inclusive state [64 x N], then aggregate state [64 x N]
     long long budget;   // clock64 cycles a single wait may take
 };
 
-// ---- the work of one CTA --------------------------------------------------------------------
-//
-// A range holds at most a tail piece of one chain (it needs the state the previous range
-// ends with), whole chains, and a head piece of another chain (its end state is needed by the
-// next range); or a middle piece of one chain.  Items run in this order: [state-only pass over
-// the piece with a successor, in pass1 mode], [head piece], [whole chains], [tail piece], so
-// the state a successor needs is published as early as possible and the state a range needs
-// is consumed as late as possible.
-
-enum : int { kInitH0 = 0, kInitZero = 1, kInitLookback = 2 };
-enum : int { kFinNone = 0, kFinFinal = 1, kFinIncl = 2, kFinAgg = 3 };
-
-struct Item {
-    int64_t u;        // unit
-    int k0, k1;       // tile range of the unit's chain
-    int pass1;        // 1: state-only pass (no y)
-    int init;         // how the state starts: kInit*
-    int fin;          // what happens to the state at the end: kFin*
-};
-
-struct Plan {
-    int n_pre;
-    Item pre[2];
-    int64_t f_lo, n_full;   // whole chains f_lo .. f_lo + n_full - 1
-    int has_post;
-    Item post;
-    int64_t n_items;
+struct Small {
+    uint64_t x_full[kXStagesMax], x_empty[kXStagesMax];   // x tile + decay slot
+    uint64_t bc_full[2], bc_empty[2];                // B / C tiles
+    uint64_t g_full[2], gp_empty[2];                 // G written / P read by Y_diag
+    // P is built by both warpgroups; each has its own barrier, because the "A" warpgroup may
+    // finish the next tile's half before the "B" warpgroup finishes this tile's half
+    uint64_t p_full_a, p_full_b;
+    uint64_t xt_full, xt_empty, s_full, s_empty, h_full, h_empty, y_full, y_empty;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    Plan plan;
 };
 
 __device__ __forceinline__ Plan make_plan(const TcParams& p, int cta) {
     Plan pl;
-    pl.n_pre = 0;
-    pl.n_full = 0;
-    pl.f_lo = 0;
-    pl.has_post = 0;
+    pl.u0 = pl.u1 = pl.f_lo = pl.n_full = pl.n_items = 0;
+    pl.k0 = pl.k1 = pl.n_pre = pl.middle = 0;
+    pl.p1 = p.pass1_mode != 0;
     const int64_t T = p.n_tiles, total = p.n_units * T;
     const int64_t start = (int64_t)cta * total / p.n_ctas;
     const int64_t end = (int64_t)(cta + 1) * total / p.n_ctas;
-    if (start >= end) {
-        pl.n_items = 0;
+    if (start >= end) return pl;
+    pl.u0 = start / T;
+    pl.u1 = (end - 1) / T;
+    pl.k0 = (int)(start % T);
+    pl.k1 = (int)((end - 1) % T + 1);
+    if (pl.u0 == pl.u1 && pl.k0 > 0 && pl.k1 < T) {     // middle piece of one chain
+        pl.middle = 1;
+        pl.n_pre = pl.p1;
+        pl.n_items = pl.n_pre + 1;
         return pl;
     }
-    const int64_t u0 = start / T, u1 = (end - 1) / T;
-    const int k0 = (int)(start % T), k1 = (int)((end - 1) % T + 1);
-    const bool p1 = p.pass1_mode != 0;
-    if (u0 == u1 && k0 > 0 && k1 < T) {              // middle piece of one chain
-        if (p1) pl.pre[pl.n_pre++] = Item{u0, k0, k1, 1, kInitZero, kFinAgg};
-        pl.post = Item{u0, k0, k1, 0, kInitLookback, kFinIncl};
-        pl.has_post = 1;
-    } else {
-        // head piece of chain u1 (starts at tile 0, ends before T)
-        const bool head = (u0 == u1) ? (k0 == 0 && k1 < T) : (k1 < T);
-        // tail piece of chain u0 (starts after tile 0, runs to T)
-        const bool tail = k0 > 0;
-        if (head) {
-            if (p1) pl.pre[pl.n_pre++] = Item{u1, 0, k1, 1, kInitH0, kFinIncl};
-            pl.pre[pl.n_pre++] = Item{u1, 0, k1, 0, kInitH0, p1 ? kFinNone : kFinIncl};
-        }
-        const int64_t f_first = tail ? u0 + 1 : u0;
-        const int64_t f_last = head ? u1 - 1 : u1;
-        if (f_last >= f_first) {
-            pl.f_lo = f_first;
-            pl.n_full = f_last - f_first + 1;
-        }
-        if (tail) {
-            pl.post = Item{u0, k0, (u0 == u1) ? k1 : (int)T, 0, kInitLookback, kFinFinal};
-            pl.has_post = 1;
-        }
+    // head piece of chain u1 (starts at tile 0, ends before T); tail piece of chain u0
+    const bool head = (pl.u0 == pl.u1) ? (pl.k0 == 0 && pl.k1 < T) : (pl.k1 < T);
+    const bool tail = pl.k0 > 0;
+    pl.n_pre = head ? 1 + pl.p1 : 0;
+    const int64_t f_first = tail ? pl.u0 + 1 : pl.u0;
+    const int64_t f_last = head ? pl.u1 - 1 : pl.u1;
+    if (f_last >= f_first) {
+        pl.f_lo = f_first;
+        pl.n_full = f_last - f_first + 1;
     }
-    pl.n_items = pl.n_pre + pl.n_full + pl.has_post;
+    pl.n_items = pl.n_pre + pl.n_full + (tail ? 1 : 0);
     return pl;
 }
 
 __device__ __forceinline__ Item plan_item(const Plan& pl, int64_t i, int T) {
-    if (i < pl.n_pre) return pl.pre[i];
+    if (pl.middle) {
+        if (pl.n_pre > 0 && i == 0) return Item{pl.u0, pl.k0, pl.k1, 1, kInitZero, kFinAgg};
+        return Item{pl.u0, pl.k0, pl.k1, 0, kInitLookback, kFinIncl};
+    }
+    if (i < pl.n_pre) {
+        if (pl.p1 && i == 0) return Item{pl.u1, 0, pl.k1, 1, kInitH0, kFinIncl};
+        return Item{pl.u1, 0, pl.k1, 0, kInitH0, pl.p1 ? kFinNone : kFinIncl};
+    }
     i -= pl.n_pre;
     if (i < pl.n_full) return Item{pl.f_lo + i, 0, T, 0, kInitH0, kFinFinal};
-    return pl.post;
-}
-
-// Position in a CTA's sequence of tiles.
-struct Cursor {
-    int64_t item;
-    int k;
-    Item it;
-    bool valid;
-};
-
-__device__ __forceinline__ Cursor first_tile(const Plan& pl, int T) {
-    Cursor c;
-    c.item = 0;
-    c.k = 0;
-    c.valid = pl.n_items > 0;
-    if (c.valid) {
-        c.it = plan_item(pl, 0, T);
-        c.k = c.it.k0;
-    }
-    return c;
-}
-
-__device__ __forceinline__ Cursor next_tile(const Plan& pl, Cursor c, int T) {
-    if (c.k + 1 < c.it.k1) {
-        ++c.k;
-        return c;
-    }
-    ++c.item;
-    c.valid = c.item < pl.n_items;
-    if (c.valid) {
-        c.it = plan_item(pl, c.item, T);
-        c.k = c.it.k0;
-    }
-    return c;
+    return Item{pl.u0, pl.k0, (pl.u0 == pl.u1) ? pl.k1 : T, 0, kInitLookback, kFinFinal};
 }
 
 struct UnitCoords {
@@ -238,6 +213,41 @@ __device__ __forceinline__ UnitCoords unit_coords(const TcParams& p, int64_t u) 
     c.b = c.bh / p.H;
     c.g = c.h / (p.H / p.G);
     return c;
+}
+
+// Position in a CTA's sequence of tiles; the unit's coordinates are refreshed only when the
+// item changes.
+struct Cursor {
+    int64_t item;
+    int k;
+    bool valid;
+    Item it;
+    UnitCoords uc;
+};
+
+__device__ __forceinline__ Cursor first_tile(const Plan& pl, const TcParams& p) {
+    Cursor c;
+    c.item = 0;
+    c.valid = pl.n_items > 0;
+    c.it = plan_item(pl, 0, p.n_tiles);
+    c.k = c.it.k0;
+    c.uc = unit_coords(p, c.valid ? c.it.u : 0);
+    return c;
+}
+
+__device__ __forceinline__ void advance(Cursor& c, const Plan& pl, const TcParams& p) {
+    if (!c.valid) return;
+    if (c.k + 1 < c.it.k1) {
+        ++c.k;
+        return;
+    }
+    ++c.item;
+    c.valid = c.item < pl.n_items;
+    if (c.valid) {
+        c.it = plan_item(pl, c.item, p.n_tiles);
+        c.k = c.it.k0;
+        c.uc = unit_coords(p, c.it.u);
+    }
 }
 
 __device__ __forceinline__ void flag_abort(Small& sm, uint8_t* ws) {
@@ -267,77 +277,223 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Small&
     return __all_sync(0xffffffffu, wait_bar(bar, parity, sm, p));
 }
 
-// Intra-warpgroup barrier on an mbarrier of count 128 (bounded, unlike bar.sync).
-__device__ __forceinline__ bool wg_sync(uint64_t* bar, uint32_t& phase, Small& sm,
-                                        const TcParams& p) {
-    mbar_arrive(bar);
-    const bool ok = wait_warp(bar, phase, sm, p);
-    phase ^= 1u;
-    return ok;
+// One 32 x 32 block (rows 32q .. 32q+31, columns 32jb .. 32jb+31) of P = L o G o dt_j.
+// Reads G's block from TMEM and writes P's block (bf16 pairs) into the upper 16 columns of the
+// same 32 columns, which only this thread's lane ever reads, so the overwrite is race-free.
+// Above the diagonal the block is zero; strictly below it every L_ij factors exactly as
+// exp(cum_i - m) exp(m - cum_j) with m = cum at row 32q - 1 (between cum_i and cum_j), so the
+// block needs no exponential; the diagonal block is masked before the exponential.
+__device__ __forceinline__ void p_block(uint32_t tg, int jb, int q, int lane, int r,
+                                        const DtSlot& sl) {
+    uint32_t pk[16];
+    if (jb > q) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+    } else {
+        float g[32];
+        tmem_ld32(tg, g);
+        if (jb < q) {
+            const float ur = sl.urow[r];
+            const float4* cf = reinterpret_cast<const float4*>(&sl.colf[q - 1][jb * 32]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 c = cf[i];
+                g[4 * i + 0] *= c.x * ur;
+                g[4 * i + 1] *= c.y * ur;
+                g[4 * i + 2] *= c.z * ur;
+                g[4 * i + 3] *= c.w * ur;
+            }
+        } else {
+            const float c2 = sl.cum2[r];
+            const float4* pc = reinterpret_cast<const float4*>(&sl.pcol[jb * 32]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 c = pc[i];
+                const float cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int jj = 4 * i + e;
+                    g[jj] = (jj <= lane) ? ex2(c2 - cv[e]) * g[jj] : 0.f;
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(g[2 * i], g[2 * i + 1]);
+    }
+    tmem_st16(tg + 16, pk);
 }
 
-// Inclusive prefix sum of `v` over the warpgroup's 128 rows (row = 32 * quarter + lane).
-// `wsum` must alternate between two buffers on consecutive calls (one barrier per scan).
-// Also returns the sum over all earlier warps (`pre`, the prefix at row 32 * quarter - 1)
-// and over the whole tile (`total`).
-__device__ __forceinline__ bool wg_scan(float& v, int quarter, int lane, float* wsum,
-                                        uint64_t* bar, uint32_t& phase, Small& sm,
-                                        const TcParams& p, float& pre, float& total) {
+// ---- the state h^T in TMEM (this thread's lane; th = lane base + first state column) ----------
+// Columns: 32-column block cb = 2 mb + half holds state rows n = 128 mb + r, columns
+// p = 32 half .. 32 half + 31.
+
+// H <- scale * src + H when `accumulate`, else H <- src.  src is a [64 x N] fp32 block (element
+// (p, n) at p * ld + n); nullptr means zeros.  `l2only` reads bypass L1 (for states another SM
+// published).
+template <int NS>
+__device__ __forceinline__ void state_from(uint32_t th, int r, const float* src, int64_t ld,
+                                           float scale, bool accumulate, bool l2only) {
+#pragma unroll 1
+    for (int cb = 0; cb < NS / 64; ++cb) {
+        const int n = (cb >> 1) * 128 + r, half = cb & 1;
+        float v[32];
+        if (accumulate) tmem_ld32(th + cb * 32, v);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
+        for (int i = 0; i < 32; ++i) {
+            float x = 0.f;
+            if (src) {
+                const float* a = src + (int64_t)(half * 32 + i) * ld + n;
+                x = l2only ? __ldcg(a) : *a;
+            }
+            v[i] = accumulate ? fmaf(scale, x, v[i]) : x;
+        }
+        tmem_st32(th + cb * 32, v);
     }
-    if (lane == 31) wsum[quarter] = v;
-    if (!wg_sync(bar, phase, sm, p)) return false;
-    pre = 0.f;
-    total = 0.f;
+}
+
+// dst[p][n] <- H (fp32)
+template <int NS>
+__device__ __forceinline__ void state_to(uint32_t th, int r, float* dst, int64_t ld) {
+#pragma unroll 1
+    for (int cb = 0; cb < NS / 64; ++cb) {
+        const int n = (cb >> 1) * 128 + r, half = cb & 1;
+        float v[32];
+        tmem_ld32(th + cb * 32, v);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float w = wsum[q];
-        if (q < quarter) pre += w;
-        total += w;
+        for (int i = 0; i < 32; ++i) dst[(int64_t)(half * 32 + i) * ld + n] = v[i];
     }
-    v += pre;
-    return true;
+}
+
+// h^T (bf16, MN-major 128-byte swizzled tile of N rows x 64 columns at shared address ht) <- H,
+// the B operand of the next off-diagonal GEMM.
+template <int NS>
+__device__ __forceinline__ void ht_from_state(uint32_t th, int r, uint32_t ht) {
+#pragma unroll 1
+    for (int cb = 0; cb < NS / 64; ++cb) {
+        const int n = (cb >> 1) * 128 + r, half = cb & 1;
+        float v[32];
+        tmem_ld32(th + cb * 32, v);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+            st_shared_v4(ht + sw128_off(n, half * 4 + cc), pack_bf16x2(v[cc * 8 + 0], v[cc * 8 + 1]),
+                         pack_bf16x2(v[cc * 8 + 2], v[cc * 8 + 3]),
+                         pack_bf16x2(v[cc * 8 + 4], v[cc * 8 + 5]),
+                         pack_bf16x2(v[cc * 8 + 6], v[cc * 8 + 7]));
+    }
+    fence_proxy_async_smem();
+}
+
+// Flags of the state hand-off between CTAs, per CTA and per "B" warp q (the warp that owns
+// state rows 32q .. 32q+31 of every 128-row block): [0] inclusive state published,
+// [1] aggregate published, [2] the aggregate's log2 decay.  A warp only needs the same rows of
+// its predecessor, so publishing and looking back are per warp, with no warpgroup barrier.
+constexpr int kFlagsPerCta = 16;
+
+// The state entering an item's first tile (per "B" warp; out of line, as it runs a few times
+// per CTA).  kInitZero: zeros; kInitH0: h0 (or zeros); kInitLookback: a decoupled look-back
+// over the preceding ranges' published states,
+//     h_in = D_1 (D_2 (... h_incl ...) + H_2) + H_1.
+// Returns false on timeout or abort.
+template <int NS>
+__device__ __noinline__ bool state_begin(const TcParams& p, Small& sm, uint32_t th, int q,
+                                         int lane, int init, const float* h0) {
+    const int r = q * 32 + lane;
+    if (init != kInitLookback) {
+        state_from<NS>(th, r, init == kInitH0 ? h0 : nullptr, p.N, 0.f, false, false);
+        return true;
+    }
+    const int64_t slot_elems = (int64_t)kPS * NS;
+    state_from<NS>(th, r, nullptr, p.N, 0.f, false, false);
+    float acc_logd = 0.f;
+    for (int jp = (int)blockIdx.x - 1; jp >= 0; --jp) {
+        const int* f = p.flags + jp * kFlagsPerCta + q * 4;
+        int kind = 0;
+        if (lane == 0) {
+            const long long t0 = clock64();
+            while (kind == 0) {
+                if (ld_acquire_gpu(f + 0)) kind = 1;
+                else if (ld_acquire_gpu(f + 1)) kind = 2;
+                else if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) break;
+                else if (clock64() - t0 > p.budget) {
+                    flag_abort(sm, p.ws);
+                    break;
+                }
+            }
+        }
+        kind = __shfl_sync(0xffffffffu, kind, 0);
+        if (kind == 0) return false;
+        // every lane acquires the flag itself before it reads the published rows
+        (void)ld_acquire_gpu(f + kind - 1);
+        const float* slot = p.slots + (int64_t)jp * 2 * slot_elems;
+        state_from<NS>(th, r, kind == 1 ? slot : slot + slot_elems, NS, ex2(acc_logd), true,
+                       true);
+        if (kind == 1) return true;
+        acc_logd += __int_as_float(__ldcg(f + 2));
+    }
+    return false;   // no inclusive state before this range: cannot happen for a valid plan
+}
+
+// The end of an item (per "B" warp, out of line): the final state into dst (kFinFinal, dst
+// may be null), or this CTA's inclusive state / aggregate published for the next range
+// (kFinIncl / kFinAgg, dst = the slot).
+template <int NS>
+__device__ __noinline__ void state_end(const TcParams& p, uint32_t th, int q, int lane, int fin,
+                                       float* dst, float item_logd) {
+    const int r = q * 32 + lane;
+    if (fin == kFinFinal) {
+        if (dst) state_to<NS>(th, r, dst, p.N);
+        return;
+    }
+    state_to<NS>(th, r, dst, NS);
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+        int* f = p.flags + (int)blockIdx.x * kFlagsPerCta + q * 4;
+        if (fin == kFinAgg) st_relaxed_gpu(f + 2, __float_as_int(item_logd));
+        st_release_gpu(f + (fin == kFinAgg ? 1 : 0), 1);
+    }
+    __syncwarp();
 }
 
 template <int NS>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
-                  const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                  const __grid_constant__ CUtensorMap tmC,
+                  const __grid_constant__ TcParams p) {
     using K = Cfg<NS>;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms and TMA destinations need 1024-byte aligned shared addresses
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     Small& sm = *reinterpret_cast<Small*>(smem + K::kOffSmall);
+    DtSlot* slots = reinterpret_cast<DtSlot*>(smem + K::kOffDt);
     const uint32_t sbase = smem_u32(smem);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int T = p.n_tiles;
-    const Plan plan = make_plan(p, blockIdx.x);
 
     if (threadIdx.x == 0) {
+        for (int i = 0; i < K::kXSt; ++i) {
+            mbar_init(&sm.x_full[i], 1 + 32);
+            mbar_init(&sm.x_empty[i], 1 + 128);
+        }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.empty[i], 1 + 128);
+            mbar_init(&sm.bc_full[i], 1);
+            mbar_init(&sm.bc_empty[i], 1);
             mbar_init(&sm.g_full[i], 1);
-            mbar_init(&sm.g_empty[i], 128);
+            mbar_init(&sm.gp_empty[i], 1);
         }
         mbar_init(&sm.xt_full, 128);
         mbar_init(&sm.xt_empty, 1);
-        mbar_init(&sm.p_full, 128);
-        mbar_init(&sm.p_empty, 1);
+        mbar_init(&sm.p_full_a, 128);
+        mbar_init(&sm.p_full_b, 128);
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.s_empty, 128);
         mbar_init(&sm.h_full, 128);
         mbar_init(&sm.h_empty, 1);
         mbar_init(&sm.y_full, 1);
         mbar_init(&sm.y_empty, 128);
-        mbar_init(&sm.a_sync, 128);
-        mbar_init(&sm.b_sync, 128);
         mbar_init(&sm.mma_done, 1);
         sm.abort_flag = 0;
+        sm.plan = make_plan(p, blockIdx.x);
         fence_mbar_init();
     }
     if (warp == kWarpMma) {
@@ -345,47 +501,151 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (warp == kWarpTma && lane == 0) {
-        prefetch_tmap(&tmX);
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmC);
     }
+    if (warp == kWarpDt && lane == 0) prefetch_tmap(&tmX);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    const Plan& plan = sm.plan;
 
     if (warp == kWarpTma) {
-        // ---------------------------------------------------------------- TMA producer ----
+        // ------------------------------------------------------- B / C TMA producer ----
         if (lane == 0) {
             int nt = 0;
-            for (Cursor c = first_tile(plan, T); c.valid; c = next_tile(plan, c, T), ++nt) {
-                const int s = nt % K::kStages;
-                const uint32_t use = nt / K::kStages;
-                if (!wait_bar(&sm.empty[s], (use & 1u) ^ 1u, sm, p)) break;
-                const UnitCoords uc = unit_coords(p, c.it.u);
+            for (Cursor c = first_tile(plan, p); c.valid; advance(c, plan, p), ++nt) {
+                const int s = nt % K::kBCStages;
+                const uint32_t use = nt / K::kBCStages;
+                if (!wait_bar(&sm.bc_empty[s], (use & 1u) ^ 1u, sm, p)) break;
                 const int t0 = c.k * kTile;
-                // a state-only tile needs x and B; a full tile also C
-                mbar_arrive_expect_tx(&sm.full[s],
-                                      c.it.pass1 ? kTileBytes * (1 + K::kNReg) : K::kStageTx);
-                tma_load_4d(smem + K::kOffX + s * kTileBytes, &tmX, &sm.full[s], uc.ps * kPS,
-                            (int)uc.h, t0, (int)uc.b);
+                const int g = (int)c.uc.g, b = (int)c.uc.b;
+                // a state-only tile needs B; a full tile also C
+                mbar_arrive_expect_tx(&sm.bc_full[s],
+                                      (c.it.pass1 ? 1 : 2) * K::kNReg * kTileBytes);
+                uint8_t* dst = smem + K::kOffBC + s * K::kBCBytes;
                 for (int r = 0; r < K::kNReg; ++r) {
-                    tma_load_4d(smem + K::kOffB + (s * K::kNReg + r) * kTileBytes, &tmB,
-                                &sm.full[s], r * 64, (int)uc.g, t0, (int)uc.b);
+                    tma_load_4d(dst + r * kTileBytes, &tmB, &sm.bc_full[s], r * 64, g, t0, b);
                     if (!c.it.pass1)
-                        tma_load_4d(smem + K::kOffC + (s * K::kNReg + r) * kTileBytes, &tmC,
-                                    &sm.full[s], r * 64, (int)uc.g, t0, (int)uc.b);
+                        tma_load_4d(dst + (K::kNReg + r) * kTileBytes, &tmC, &sm.bc_full[s],
+                                    r * 64, g, t0, b);
                 }
             }
             if (sm.abort_flag) {
                 // drain: every issued load must land before the CTA's smem goes away
                 const long long t0 = clock64();
-                for (int j = nt - K::kStages; j < nt; ++j) {
+                for (int j = nt - K::kBCStages; j < nt; ++j) {
                     if (j < 0) continue;
-                    const int s = j % K::kStages;
-                    const uint32_t use = j / K::kStages;
-                    while (!mbar_try_wait(&sm.full[s], use & 1u) && clock64() - t0 < p.budget) {
+                    const int s = j % K::kBCStages;
+                    const uint32_t use = j / K::kBCStages;
+                    while (!mbar_try_wait(&sm.bc_full[s], use & 1u) &&
+                           clock64() - t0 < p.budget) {
                     }
+                }
+            }
+        }
+    } else if (warp == kWarpDt) {
+        // ------------------------------------------ x TMA + decay-factor producer ----
+        // dt of the tile two ahead is loaded into registers while this tile is computed.
+        auto load_dt = [&](const Cursor& c, float (&v)[4]) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = 0.f;
+            if (!c.valid) return;
+            const int64_t t = (int64_t)c.k * kTile + 4 * lane;
+            const __nv_bfloat16* src = p.dt + (c.uc.b * p.L + t) * p.H + c.uc.h;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (t + i < p.L) v[i] = __bfloat162float(src[(int64_t)i * p.H]);
+        };
+        Cursor c = first_tile(plan, p);
+        Cursor cl = c;
+        float d0[4], d1[4];
+        load_dt(cl, d0);
+        advance(cl, plan, p);
+        load_dt(cl, d1);
+        advance(cl, plan, p);
+        int nt = 0;
+        int64_t a_u = -1;
+        float A2 = 0.f;
+        for (; c.valid; advance(c, plan, p), ++nt) {
+            float d2[4];
+            load_dt(cl, d2);
+            advance(cl, plan, p);
+            const int s = nt % K::kXSt;
+            const uint32_t use = nt / K::kXSt;
+            if (!wait_warp(&sm.x_empty[s], (use & 1u) ^ 1u, sm, p)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&sm.x_full[s], kTileBytes);
+                tma_load_4d(smem + K::kOffX + s * kTileBytes, &tmX, &sm.x_full[s],
+                            c.uc.ps * kPS, (int)c.uc.h, c.k * kTile, (int)c.uc.b);
+            }
+            if (c.it.u != a_u) {
+                a_u = c.it.u;
+                A2 = p.A[c.uc.h] * kLog2e;
+            }
+            // log2-domain cumsum: 4 consecutive tokens per lane, then a warp scan
+            float cs[4];
+            cs[0] = d0[0] * A2;
+#pragma unroll
+            for (int i = 1; i < 4; ++i) cs[i] = fmaf(d0[i], A2, cs[i - 1]);
+            float incl = cs[3];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+            if (lane == 0) excl = 0.f;
+            const float clast2 = __shfl_sync(0xffffffffu, incl, 31);
+            const float m1 = __shfl_sync(0xffffffffu, incl, 7);    // cum2 at token 31
+            const float m2 = __shfl_sync(0xffffffffu, incl, 15);   // token 63
+            const float m3 = __shfl_sync(0xffffffffu, incl, 23);   // token 95
+            const int q = lane >> 3;
+            const float mq = q == 1 ? m1 : (q == 2 ? m2 : m3);
+            float v_c[4], v_p[4], v_w[4], v_e[4], v_u[4], v_f1[4], v_f2[4], v_f3[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float c2 = excl + cs[i];
+                const float pc = d0[i] > 0.f ? c2 - lg2(d0[i]) : __int_as_float(0x7f800000);
+                v_c[i] = c2;
+                v_p[i] = pc;
+                v_w[i] = ex2(clast2 - c2) * d0[i];
+                v_e[i] = ex2(c2);
+                v_u[i] = q > 0 ? ex2(c2 - mq) : 1.f;
+                v_f1[i] = ex2(m1 - pc);
+                v_f2[i] = ex2(m2 - pc);
+                v_f3[i] = ex2(m3 - pc);
+            }
+            DtSlot& sl = slots[s];
+            const int o = 4 * lane;
+            *reinterpret_cast<float4*>(&sl.cum2[o]) = make_float4(v_c[0], v_c[1], v_c[2], v_c[3]);
+            *reinterpret_cast<float4*>(&sl.pcol[o]) = make_float4(v_p[0], v_p[1], v_p[2], v_p[3]);
+            *reinterpret_cast<float4*>(&sl.w[o]) = make_float4(v_w[0], v_w[1], v_w[2], v_w[3]);
+            *reinterpret_cast<float4*>(&sl.e[o]) = make_float4(v_e[0], v_e[1], v_e[2], v_e[3]);
+            *reinterpret_cast<float4*>(&sl.urow[o]) = make_float4(v_u[0], v_u[1], v_u[2], v_u[3]);
+            *reinterpret_cast<float4*>(&sl.colf[0][o]) =
+                make_float4(v_f1[0], v_f1[1], v_f1[2], v_f1[3]);
+            *reinterpret_cast<float4*>(&sl.colf[1][o]) =
+                make_float4(v_f2[0], v_f2[1], v_f2[2], v_f2[3]);
+            *reinterpret_cast<float4*>(&sl.colf[2][o]) =
+                make_float4(v_f3[0], v_f3[1], v_f3[2], v_f3[3]);
+            if (lane == 0) sl.clast2 = clast2;
+            mbar_arrive(&sm.x_full[s]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                d0[i] = d1[i];
+                d1[i] = d2[i];
+            }
+        }
+        if (sm.abort_flag && lane == 0) {
+            // drain: the x loads of every tile this loop completed must land before exit
+            const long long t0 = clock64();
+            for (int j = nt - K::kXSt; j < nt; ++j) {
+                if (j < 0) continue;
+                const int s = j % K::kXSt;
+                const uint32_t use = j / K::kXSt;
+                while (!mbar_try_wait(&sm.x_full[s], use & 1u) && clock64() - t0 < p.budget) {
                 }
             }
         }
@@ -398,15 +658,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idYd = idesc_bf16(128, kPS, 0, 1);
             // G = C B^T of tile number nt (the j-th full tile) into G buffer j % kGBuf
             auto issue_G = [&](int nt, int j) -> bool {
-                const int s = nt % K::kStages;
+                const int s = nt % K::kBCStages;
                 const int gb = j % K::kGBuf;
-                if (!wait_bar(&sm.full[s], (uint32_t)(nt / K::kStages) & 1u, sm, p)) return false;
-                if (!wait_bar(&sm.g_empty[gb], ((uint32_t)(j / K::kGBuf) & 1u) ^ 1u, sm, p))
+                if (!wait_bar(&sm.bc_full[s], (uint32_t)(nt / K::kBCStages) & 1u, sm, p))
+                    return false;
+                if (!wait_bar(&sm.gp_empty[gb], ((uint32_t)(j / K::kGBuf) & 1u) ^ 1u, sm, p))
                     return false;
                 tc_fence_after();
-                const uint32_t cbase = sbase + K::kOffC + s * K::kNReg * kTileBytes;
-                const uint32_t bbase = sbase + K::kOffB + s * K::kNReg * kTileBytes;
-#pragma unroll
+                const uint32_t bbase = sbase + K::kOffBC + s * K::kBCBytes;
+                const uint32_t cbase = bbase + K::kNReg * kTileBytes;
+#pragma unroll 1
                 for (int kk = 0; kk < NS / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
                     mma_f16(tmem + K::kColG + gb * 128, smem_desc_sw128(cbase + off, 16, 1024),
@@ -417,24 +678,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             int nt = 0, j = 0;           // tiles issued, full (non state-only) tiles issued
             bool g_ahead = false;        // G of the current tile was issued one tile early
-            for (Cursor c = first_tile(plan, T); c.valid; c = next_tile(plan, c, T), ++nt) {
-                const int s = nt % K::kStages;
+            Cursor c = first_tile(plan, p);
+            for (; c.valid; ++nt) {
+                Cursor nx = c;
+                advance(nx, plan, p);
+                const int s = nt % K::kBCStages;
+                const int xs = nt % K::kXSt;
                 const uint32_t par = (uint32_t)nt & 1u;
                 const bool full_tile = !c.it.pass1;
-                const Cursor nx = next_tile(plan, c, T);
                 const bool next_full = nx.valid && !nx.it.pass1;
                 if (full_tile && !g_ahead && !issue_G(nt, j)) break;
                 g_ahead = false;
                 // chunk state S^T = B^T (w o X)
                 if (!wait_bar(&sm.xt_full, par, sm, p) || !wait_bar(&sm.s_empty, par ^ 1u, sm, p))
                     break;
+                if (!full_tile &&
+                    !wait_bar(&sm.bc_full[s], (uint32_t)(nt / K::kBCStages) & 1u, sm, p))
+                    break;
                 tc_fence_after();
                 {
-                    const uint32_t bbase = sbase + K::kOffB + s * K::kNReg * kTileBytes;
+                    const uint32_t bbase = sbase + K::kOffBC + s * K::kBCBytes;
                     const uint32_t xt = sbase + K::kOffXt;
-#pragma unroll
+#pragma unroll 1
                     for (int mb = 0; mb < K::kMB; ++mb)
-#pragma unroll
+#pragma unroll 1
                         for (int kk = 0; kk < kTile / 16; ++kk)
                             mma_f16(tmem + K::kColS + mb * kPS,
                                     smem_desc_sw128(bbase + 2 * mb * kTileBytes + kk * 2048,
@@ -444,18 +711,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&sm.s_full);
                 mma_commit(&sm.xt_empty);
                 if (!full_tile) {
-                    mma_commit(&sm.empty[s]);
+                    mma_commit(&sm.bc_empty[s]);
+                    mma_commit(&sm.x_empty[xs]);
+                    c = nx;
                     continue;
                 }
                 const uint32_t jpar = (uint32_t)j & 1u;
+                const int gb = j % K::kGBuf;
                 // off-diagonal Y_off = C h_prev^T
                 if (!wait_bar(&sm.h_full, jpar, sm, p) || !wait_bar(&sm.y_empty, jpar ^ 1u, sm, p))
                     break;
                 tc_fence_after();
                 {
-                    const uint32_t cbase = sbase + K::kOffC + s * K::kNReg * kTileBytes;
+                    const uint32_t cbase = sbase + K::kOffBC + s * K::kBCBytes +
+                                           K::kNReg * kTileBytes;
                     const uint32_t ht = sbase + K::kOffHt;
-#pragma unroll
+#pragma unroll 1
                     for (int kk = 0; kk < NS / 16; ++kk)
                         mma_f16(tmem + K::kColYoff,
                                 smem_desc_sw128(cbase + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16,
@@ -463,33 +734,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 smem_desc_sw128(ht + kk * 2048, 1024, 1024), idYoff, kk > 0);
                 }
                 mma_commit(&sm.h_empty);
-                // next tile's C B^T while the A warpgroup builds this tile's P (with a single
-                // smem stage the next tile can only land after this tile releases it, below)
-                if (K::kStages > 1 && next_full) {
+                mma_commit(&sm.bc_empty[s]);   // G, S^T and Y_off have read this B / C stage
+                // next tile's C B^T while this tile's P is built
+                if (K::kBCStages > 1 && next_full) {
                     if (!issue_G(nt + 1, j + 1)) break;
                     g_ahead = true;
                 }
-                // Y_diag = P X
-                if (!wait_bar(&sm.p_full, jpar, sm, p)) break;
+                // Y_diag = P X, P read from TMEM (upper 16 of each 32 G columns)
+                if (!wait_bar(&sm.p_full_a, jpar, sm, p) || !wait_bar(&sm.p_full_b, jpar, sm, p))
+                    break;
                 tc_fence_after();
                 {
-                    const uint32_t pb = sbase + K::kOffP;
-                    const uint32_t xb = sbase + K::kOffX + s * kTileBytes;
-#pragma unroll
+                    const uint32_t pcol = tmem + K::kColG + gb * 128 + 16;
+                    const uint32_t xb = sbase + K::kOffX + xs * kTileBytes;
+#pragma unroll 1
                     for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_f16(tmem + K::kColY,
-                                smem_desc_sw128(pb + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16,
-                                                1024),
-                                smem_desc_sw128(xb + kk * 2048, 1024, 1024), idYd, kk > 0);
+                        mma_f16_ts(tmem + K::kColY, pcol + (kk >> 1) * 32 + (kk & 1) * 8,
+                                   smem_desc_sw128(xb + kk * 2048, 1024, 1024), idYd, kk > 0);
                 }
-                mma_commit(&sm.p_empty);
                 mma_commit(&sm.y_full);
-                mma_commit(&sm.empty[s]);
-                if (K::kStages == 1 && next_full) {
+                mma_commit(&sm.gp_empty[gb]);
+                mma_commit(&sm.x_empty[xs]);
+                if (K::kBCStages == 1 && next_full) {
                     if (!issue_G(nt + 1, j + 1)) break;
                     g_ahead = true;
                 }
                 ++j;
+                c = nx;
             }
             // every MMA issued above has completed once this barrier's phase 0 completes
             mma_commit(&sm.mma_done);
@@ -501,39 +772,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- "A" warpgroup ---
         const int q = warp & 3;                 // TMEM lane quarter
         const int r = q * 32 + lane;            // tile row
-        uint32_t sync_phase = 0;
-        auto load_dt = [&](const Cursor& c) -> float {
-            if (!c.valid) return 0.f;
-            const UnitCoords uc = unit_coords(p, c.it.u);
-            const int64_t t = (int64_t)c.k * kTile + r;
-            return t < p.L ? __bfloat162float(p.dt[(uc.b * p.L + t) * p.H + uc.h]) : 0.f;
-        };
-        Cursor c = first_tile(plan, T);
-        float dt_next = load_dt(c);
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int nt = 0, j = 0;
-        for (; c.valid; ++nt) {
-            const Cursor nx = next_tile(plan, c, T);
-            const int s = nt % K::kStages;
+        for (Cursor c = first_tile(plan, p); c.valid; advance(c, plan, p), ++nt) {
+            const int xs = nt % K::kXSt;
             const uint32_t par = (uint32_t)nt & 1u;
             const bool full_tile = !c.it.pass1;
-            const float dtv = dt_next;           // loaded one tile ahead
-            dt_next = load_dt(nx);
-            const float A2 = p.A[unit_coords(p, c.it.u).h] * kLog2e;
-            float c2 = dtv * A2;                // log2-domain cumsum
-            float pre, clast2;
-            if (!wg_scan(c2, q, lane, sm.a_wsum[par], &sm.a_sync, sync_phase, sm, p, pre, clast2))
-                break;
-            if (full_tile) {
-                sm.a_cp[r] = c2 - lg2(dtv);     // folds dt_j into the column term (+inf if 0)
-                if (!wg_sync(&sm.a_sync, sync_phase, sm, p)) break;
-            }
-
+            if (!wait_warp(&sm.x_full[xs], (uint32_t)(nt / K::kXSt) & 1u, sm, p)) break;
+            const DtSlot& sl = slots[xs];
             // w o X for the chunk-state GEMM: row r scaled by exp(cum_last - cum_r) dt_r
-            if (!wait_warp(&sm.full[s], (uint32_t)(nt / K::kStages) & 1u, sm, p)) break;
             if (!wait_warp(&sm.xt_empty, par ^ 1u, sm, p)) break;
             {
-                const float wr = ex2(clast2 - c2) * dtv;
-                const uint32_t xrow = sbase + K::kOffX + s * kTileBytes;
+                const float wr = sl.w[r];
+                const uint32_t xrow = sbase + K::kOffX + xs * kTileBytes;
                 const uint32_t xtrow = sbase + K::kOffXt;
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
@@ -549,259 +800,114 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(&sm.xt_full);
-
             if (full_tile) {
-                // P = L o G o dt_j (bf16, K-major swizzled), L masked before exp.
-                // Below the warp's diagonal 32x32 block every L_ij factors exactly as
-                // exp(cum_i - m) * exp(m - cum_j), m = cum at row 32q - 1, which lies between
-                // cum_i and cum_j, so those blocks need one exponential per row and one per
-                // column instead of one per element.
+                // column blocks 0 and 1 of P (the "B" warpgroup builds blocks 2 and 3)
                 const int gb = j % K::kGBuf;
-                const uint32_t jpar = (uint32_t)j & 1u;
-                if (!wait_warp(&sm.p_empty, jpar ^ 1u, sm, p)) break;
                 if (!wait_warp(&sm.g_full[gb], (uint32_t)(j / K::kGBuf) & 1u, sm, p)) break;
                 tc_fence_after();
-                const uint32_t prow = sbase + K::kOffP;
-                const float u_r = ex2(c2 - pre);    // exp(cum_r - m)
-#pragma unroll
-                for (int jb = 0; jb < 4; ++jb) {
-                    const uint32_t atom = prow + (jb >> 1) * kTileBytes;
-                    if (jb > q) {   // strictly above the diagonal for the whole warp
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc)
-                            st_shared_v4(atom + sw128_off(r, (jb & 1) * 4 + cc), 0, 0, 0, 0);
-                        continue;
-                    }
-                    float gv[32];
-                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + K::kColG + gb * 128 + jb * 32,
-                              gv);
-                    if (jb < q) {
-                        // column factor exp(m - cum_j) dt_j, one per lane, shared by shuffles
-                        const float wl = ex2(pre - sm.a_cp[jb * 32 + lane]);
-#pragma unroll
-                        for (int jj = 0; jj < 32; ++jj)
-                            gv[jj] *= __shfl_sync(0xffffffffu, wl, jj) * u_r;
-                    } else {
-#pragma unroll
-                        for (int jj = 0; jj < 32; ++jj)
-                            gv[jj] = (jj <= lane) ? ex2(c2 - sm.a_cp[jb * 32 + jj]) * gv[jj] : 0.f;
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        st_shared_v4(atom + sw128_off(r, (jb & 1) * 4 + cc),
-                                     pack_bf16x2(gv[cc * 8 + 0], gv[cc * 8 + 1]),
-                                     pack_bf16x2(gv[cc * 8 + 2], gv[cc * 8 + 3]),
-                                     pack_bf16x2(gv[cc * 8 + 4], gv[cc * 8 + 5]),
-                                     pack_bf16x2(gv[cc * 8 + 6], gv[cc * 8 + 7]));
-                }
+                const uint32_t tg = tmem + lane_base + K::kColG + gb * 128;
+#pragma unroll 1
+                for (int jb = 0; jb < 2; ++jb) p_block(tg + jb * 32, jb, q, lane, r, sl);
+                tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&sm.g_empty[gb]);
-                fence_proxy_async_smem();
-                mbar_arrive(&sm.p_full);
+                mbar_arrive(&sm.p_full_a);
                 ++j;
             }
-            c = nx;
         }
     } else {
         // ---------------------------------------------------------------- "B" warpgroup ---
+        // The state h^T (rows n = 128 mb + r, columns p) lives in TMEM columns kColH + 64 mb.
         const int q = warp & 3;
         const int r = q * 32 + lane;             // tile row, and state row inside a 128-block
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        const int64_t slot_elems = (int64_t)kPS * NS;
-        uint32_t sync_phase = 0;
-        bool ok = true;
-        auto load_dt = [&](const Cursor& c) -> float {
-            if (!c.valid) return 0.f;
-            const UnitCoords uc = unit_coords(p, c.it.u);
-            const int64_t t = (int64_t)c.k * kTile + r;
-            return t < p.L ? __bfloat162float(p.dt[(uc.b * p.L + t) * p.H + uc.h]) : 0.f;
-        };
-        // H (TMEM) <- scale * src + H when `accumulate`, else H <- src.  src is a [64 x N] fp32
-        // block (element (p, n) at p * ld + n); nullptr means zeros.  `l2only` reads bypass L1
-        // (for states another SM published).
-        auto h_from = [&](const float* src, int64_t ld, float scale, bool accumulate,
-                          bool l2only) {
-#pragma unroll
-            for (int mb = 0; mb < K::kMB; ++mb) {
-                const int n = mb * 128 + r;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float v[32];
-                    if (accumulate)
-                        tmem_ld32(tmem + lane_base + K::kColH + mb * kPS + half * 32, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x = 0.f;
-                        if (src) {
-                            const float* a = src + (int64_t)(half * 32 + i) * ld + n;
-                            x = l2only ? __ldcg(a) : *a;
-                        }
-                        v[i] = accumulate ? fmaf(scale, x, v[i]) : x;
-                    }
-                    tmem_st32(tmem + lane_base + K::kColH + mb * kPS + half * 32, v);
-                }
-            }
-        };
-        // dst[p][n] <- H (fp32)
-        auto h_to = [&](float* dst, int64_t ld) {
-#pragma unroll
-            for (int mb = 0; mb < K::kMB; ++mb) {
-                const int n = mb * 128 + r;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float hv[32];
-                    tmem_ld32(tmem + lane_base + K::kColH + mb * kPS + half * 32, hv);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) dst[(int64_t)(half * 32 + i) * ld + n] = hv[i];
-                }
-            }
-        };
-        // h^T (bf16, MN-major swizzled) <- H, for the next Y_off GEMM
-        auto ht_from_h = [&]() {
-#pragma unroll
-            for (int mb = 0; mb < K::kMB; ++mb) {
-                const int n = mb * 128 + r;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float hv[32];
-                    tmem_ld32(tmem + lane_base + K::kColH + mb * kPS + half * 32, hv);
-                    const uint32_t hrow = sbase + K::kOffHt;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        st_shared_v4(hrow + sw128_off(n, half * 4 + cc),
-                                     pack_bf16x2(hv[cc * 8 + 0], hv[cc * 8 + 1]),
-                                     pack_bf16x2(hv[cc * 8 + 2], hv[cc * 8 + 3]),
-                                     pack_bf16x2(hv[cc * 8 + 4], hv[cc * 8 + 5]),
-                                     pack_bf16x2(hv[cc * 8 + 6], hv[cc * 8 + 7]));
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&sm.h_full);
-        };
-        Cursor c = first_tile(plan, T);
-        float dt_next = load_dt(c);
+        const uint32_t th = tmem + lane_base + K::kColH;
         int nt = 0, j = 0;
-        int64_t cur_item = -1;
+        int64_t b_u = -1;
+        float Dh = 0.f;
         float item_logd = 0.f;                   // sum of log2 tile decays over the item
-        for (; c.valid && ok; ++nt) {
-            const Cursor nx = next_tile(plan, c, T);
-            const UnitCoords uc = unit_coords(p, c.it.u);
+        Cursor c = first_tile(plan, p);
+        for (; c.valid; ++nt) {
+            Cursor nx = c;
+            advance(nx, plan, p);
+            const UnitCoords& uc = c.uc;
             const bool full_tile = !c.it.pass1;
-            const int s = nt % K::kStages;
+            const int xs = nt % K::kXSt;
             const uint32_t par = (uint32_t)nt & 1u;
-            if (c.item != cur_item) {
+            if (c.k == c.it.k0) {
                 // ---- start of an item: the state entering its first tile
-                cur_item = c.item;
                 item_logd = 0.f;
-                const int64_t hbase = (uc.bh * p.P + (int64_t)uc.ps * kPS) * p.N;
-                if (c.it.init == kInitZero) {
-                    h_from(nullptr, p.N, 0.f, false, false);
-                } else if (c.it.init == kInitH0) {
-                    h_from(p.h0 ? p.h0 + hbase : nullptr, p.N, 0.f, false, false);
-                } else {
-                    // decoupled look-back over the preceding ranges' published states:
-                    // h_in = D_1 (D_2 (... h_incl ...) + H_2) + H_1
-                    h_from(nullptr, p.N, 0.f, false, false);
-                    float acc_logd = 0.f;
-                    int jp = (int)blockIdx.x - 1;
-                    while (true) {
-                        if (r == 0) {
-                            int kind = 0;
-                            const long long t0 = clock64();
-                            while (jp >= 0 && kind == 0) {
-                                if (ld_acquire_gpu(p.flags + 4 * jp + 0)) kind = 1;
-                                else if (ld_acquire_gpu(p.flags + 4 * jp + 1)) kind = 2;
-                                else if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) break;
-                                else if (clock64() - t0 > p.budget) {
-                                    flag_abort(sm, p.ws);
-                                    break;
-                                }
-                            }
-                            sm.lb_kind = kind;
-                            sm.lb_logd = kind == 2 ? __int_as_float(__ldcg(p.flags + 4 * jp + 2))
-                                                   : 0.f;
-                        }
-                        if (!wg_sync(&sm.b_sync, sync_phase, sm, p)) {
-                            ok = false;
-                            break;
-                        }
-                        const int kind = sm.lb_kind;
-                        const float lb_logd = sm.lb_logd;
-                        if (!wg_sync(&sm.b_sync, sync_phase, sm, p)) {   // lb_* consumed
-                            ok = false;
-                            break;
-                        }
-                        if (kind == 0) {
-                            ok = false;
-                            break;
-                        }
-                        const float* slot = p.slots + (int64_t)jp * 2 * slot_elems;
-                        h_from(kind == 1 ? slot : slot + slot_elems, NS, ex2(acc_logd), true,
-                               true);
-                        if (kind == 1) break;
-                        acc_logd += lb_logd;
-                        --jp;
-                    }
-                    if (!ok) break;
+                if (c.it.u != b_u) {
+                    b_u = c.it.u;
+                    Dh = p.D ? p.D[uc.h] : 0.f;
                 }
+                const int64_t hbase = (uc.bh * p.P + (int64_t)uc.ps * kPS) * p.N;
+                if (!state_begin<NS>(p, sm, th, q, lane, c.it.init,
+                                     p.h0 ? p.h0 + hbase : nullptr))
+                    break;
                 if (full_tile) {
                     // h^T for the item's first Y_off, once the previous full tile's Y_off is done
                     if (j > 0 && !wait_warp(&sm.h_empty, (uint32_t)(j - 1) & 1u, sm, p)) break;
-                    ht_from_h();
+                    ht_from_state<NS>(th, r, sbase + K::kOffHt);
+                    mbar_arrive(&sm.h_full);
                 }
             }
-            const float dtv = dt_next;           // loaded one tile ahead
-            dt_next = load_dt(nx);
-            const float A2 = p.A[uc.h] * kLog2e;
-            const float Dh = p.D ? p.D[uc.h] : 0.f;
-            float c2 = dtv * A2;
-            float pre, clast2;
-            if (!wg_scan(c2, q, lane, sm.b_wsum[par], &sm.b_sync, sync_phase, sm, p, pre, clast2))
-                break;
-            const float e_r = ex2(c2);          // exp(cum_r)
+            if (!wait_warp(&sm.x_full[xs], (uint32_t)(nt / K::kXSt) & 1u, sm, p)) break;
+            const DtSlot& sl = slots[xs];
+            const float clast2 = sl.clast2;
             const float decay = ex2(clast2);    // exp(cum_last)
             item_logd += clast2;
+            const int gb = j % K::kGBuf;
+            const uint32_t jpar = (uint32_t)j & 1u;
+
+            if (full_tile) {
+                // column blocks 2 and 3 of P
+                if (!wait_warp(&sm.g_full[gb], (uint32_t)(j / K::kGBuf) & 1u, sm, p)) break;
+                tc_fence_after();
+                const uint32_t tg = tmem + lane_base + K::kColG + gb * 128;
+#pragma unroll 1
+                for (int jb = 2; jb < 4; ++jb) p_block(tg + jb * 32, jb, q, lane, r, sl);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sm.p_full_b);
+            }
 
             // S3: H = exp(cum_last) H + S^T
             if (!wait_warp(&sm.s_full, par, sm, p)) break;
             tc_fence_after();
+#pragma unroll 1
+            for (int cb = 0; cb < 2 * K::kMB; ++cb) {
+                float sv[32], hv[32];
+                tmem_ld32x2(tmem + lane_base + K::kColS + cb * 32, sv, th + cb * 32, hv);
 #pragma unroll
-            for (int mb = 0; mb < K::kMB; ++mb)
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float sv[32], hv[32];
-                    tmem_ld32(tmem + lane_base + K::kColS + mb * kPS + half * 32, sv);
-                    tmem_ld32(tmem + lane_base + K::kColH + mb * kPS + half * 32, hv);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) hv[i] = fmaf(decay, hv[i], sv[i]);
-                    tmem_st32(tmem + lane_base + K::kColH + mb * kPS + half * 32, hv);
-                }
+                for (int i = 0; i < 32; ++i) hv[i] = fmaf(decay, hv[i], sv[i]);
+                tmem_st32(th + cb * 32, hv);
+            }
             tc_fence_before();
             mbar_arrive(&sm.s_empty);
             const bool last_of_item = !nx.valid || nx.item != c.item;
 
             if (full_tile) {
-                const uint32_t jpar = (uint32_t)j & 1u;
                 // h^T for the next tile's Y_off, once this tile's Y_off has read the old one
                 if (!last_of_item) {
                     if (!wait_warp(&sm.h_empty, jpar, sm, p)) break;
-                    ht_from_h();
+                    ht_from_state<NS>(th, r, sbase + K::kOffHt);
+                    mbar_arrive(&sm.h_full);
                 }
                 // S4: y = Y_diag + exp(cum) Y_off + D x
                 if (!wait_warp(&sm.y_full, jpar, sm, p)) break;
-                if (!wait_warp(&sm.full[s], (uint32_t)(nt / K::kStages) & 1u, sm, p)) break;
                 tc_fence_after();
+                const float e_r = sl.e[r];
                 const int64_t t = (int64_t)c.k * kTile + r;
-                const uint32_t xrow = sbase + K::kOffX + s * kTileBytes;
+                const uint32_t xrow = sbase + K::kOffX + xs * kTileBytes;
                 __nv_bfloat16* yrow = p.y + ((uc.b * p.L + t) * p.H + uc.h) * p.P + uc.ps * kPS;
+#pragma unroll 1
+                for (int qc = 0; qc < 4; ++qc) {
+                    float yd[16], yo[16];
+                    tmem_ld16x2(tmem + lane_base + K::kColY + qc * 16, yd,
+                                tmem + lane_base + K::kColYoff + qc * 16, yo);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float yd[32], yo[32];
-                    tmem_ld32(tmem + lane_base + K::kColY + half * 32, yd);
-                    tmem_ld32(tmem + lane_base + K::kColYoff + half * 32, yo);
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const uint4 xv = ld_shared_v4(xrow + sw128_off(r, half * 4 + cc));
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const uint4 xv = ld_shared_v4(xrow + sw128_off(r, qc * 2 + cc));
                         const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
                         uint32_t o[4];
 #pragma unroll
@@ -814,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             o[e] = pack_bf16x2(v0, v1);
                         }
                         if (t < p.L)
-                            *reinterpret_cast<uint4*>(yrow + half * 32 + cc * 8) =
+                            *reinterpret_cast<uint4*>(yrow + qc * 16 + cc * 8) =
                                 make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 }
@@ -822,43 +928,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&sm.y_empty);
                 ++j;
             }
-            mbar_arrive(&sm.empty[s]);
+            mbar_arrive(&sm.x_empty[xs]);
 
-            if (last_of_item) {
+            if (last_of_item && c.it.fin != kFinNone) {
                 // ---- end of an item: final state, or publish for the next range
-                const int fin = c.it.fin;
-                if (fin == kFinFinal) {
-                    if (p.hT) h_to(p.hT + (uc.bh * p.P + (int64_t)uc.ps * kPS) * p.N, p.N);
-                } else if (fin == kFinIncl || fin == kFinAgg) {
-                    float* slot = p.slots + (int64_t)blockIdx.x * 2 * slot_elems +
-                                  (fin == kFinAgg ? slot_elems : 0);
-                    h_to(slot, NS);
-                    __threadfence();
-                    if (!wg_sync(&sm.b_sync, sync_phase, sm, p)) break;
-                    if (r == 0) {
-                        if (fin == kFinAgg)
-                            st_relaxed_gpu(p.flags + 4 * blockIdx.x + 2, __float_as_int(item_logd));
-                        st_release_gpu(p.flags + 4 * blockIdx.x + (fin == kFinAgg ? 1 : 0), 1);
-                    }
+                float* dst = nullptr;
+                if (c.it.fin == kFinFinal) {
+                    if (p.hT) dst = p.hT + (uc.bh * p.P + (int64_t)uc.ps * kPS) * p.N;
+                } else {
+                    dst = p.slots + (int64_t)blockIdx.x * 2 * kPS * NS +
+                          (c.it.fin == kFinAgg ? kPS * NS : 0);
                 }
+                state_end<NS>(p, th, q, lane, c.it.fin, dst, item_logd);
             }
             c = nx;
         }
     }
 
+    // single-lane roles (TMA, MMA issue) reconverge their warp before the CTA barrier
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kWarpMma) {
-        __syncwarp();
-        tmem_dealloc(tmem, kTmemCols);
-    }
+    if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int NS>
 constexpr size_t smem_bytes() {
     return Cfg<NS>::kOffSmall + sizeof(Small) + 1024;   // + alignment slack
 }
+// at most 227 KB of dynamic shared memory per CTA on sm_103a
+static_assert(smem_bytes<128>() <= 232448 && smem_bytes<256>() <= 232448, "shared memory");
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -888,7 +988,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
            CUDA_SUCCESS;
 }
 
-size_t flags_bytes() { return align_up(sizeof(int) * 4 * kMaxCtas, 256); }
+size_t flags_bytes() { return align_up(sizeof(int) * kFlagsPerCta * kMaxCtas, 256); }
 size_t slots_bytes(int64_t N) { return sizeof(float) * 2 * (size_t)kMaxCtas * kPS * (size_t)N; }
 
 int sm_count() {
@@ -931,7 +1031,8 @@ int launch_ns(const ScanArgs& a) {
     p.flags = reinterpret_cast<int*>(a.ws + kWsHeaderBytes);
     p.slots = reinterpret_cast<float*>(a.ws + kWsHeaderBytes + flags_bytes());
     p.budget = 4ll << 30;   // ~2 s at the B300's maximum SM clock
-    if (cudaMemsetAsync(p.flags, 0, sizeof(int) * 4 * (size_t)p.n_ctas, a.stream) != cudaSuccess)
+    if (cudaMemsetAsync(p.flags, 0, sizeof(int) * kFlagsPerCta * (size_t)p.n_ctas, a.stream) !=
+        cudaSuccess)
         return SSD_ERR_CUDA;
     const size_t smem = smem_bytes<NS>();
     if (cudaFuncSetAttribute(ssd_tc_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
