@@ -6,10 +6,10 @@
 //
 //   S1  cum_i = sum_{k<=i} dt_k A  (inside the tile); L_ij = exp(cum_i - cum_j) for i >= j
 //   S2  G = C B^T                         tcgen05.mma  M=128 N=128 K=d_state   (TMEM)
-//       P = L o G o dt_j  -> bf16, written back into G's TMEM columns (CUDA cores, mask first)
+//       P = L o G o dt_j  -> bf16 in TMEM (CUDA cores, mask first, then exp)
 //       Y_diag = P X                      tcgen05.mma  A = P from TMEM, M=128 N=64 K=128
 //       S^T = B^T (diag(exp(cum_last - cum) dt) X)   M=d_state N=64 K=128
-//   S3  H = exp(cum_last) H + S^T         CUDA cores, H (= h^T, fp32) lives in TMEM
+//   S3  H = exp(cum_last) H + S^T         CUDA cores, H (= h^T, fp32) in registers
 //   S4  Y_off = C h_prev^T                tcgen05.mma  M=128 N=64  K=d_state
 //       y = Y_diag + exp(cum) Y_off + D x -> bf16, 16-byte stores
 //
@@ -28,12 +28,14 @@
 // Warp roles (352 threads):
 //   warp 0      TMA producer of the B / C ring (2 stages for d_state 128)
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
-//   warp 2      producer of the x / decay ring: TMA of the x tile, and from dt (loaded two tiles
-//               ahead) the tile's log2-domain cumsum and every exponential factor the other
-//               roles need (3 stages)
-//   warps 3-6   "A" warpgroup: scaled copy of x for the state GEMM, half of P = L o G
-//   warps 7-10  "B" warpgroup: the other half of P, state recurrence, bf16 h^T for the next
-//               tile's off-diagonal GEMM, y epilogue, state hand-off between CTAs
+//   warp 2      producer of the x / decay ring: TMA of the x tile, and from dt the tile's
+//               log2-domain cumsum and every exponential factor the other roles need
+//   warps 3-10  two identical compute warpgroups; warpgroup g (warps 3+4g .. 6+4g) owns
+//               headdim columns 32g .. 32g+31 of x, the state and y, and half of P's column
+//               blocks.  Per tile: scaled copy of x for the state GEMM, its P blocks, the
+//               state recurrence in registers and bf16 h^T for the next off-diagonal GEMM;
+//               the y epilogue of a tile runs one tile later, so the tensor core never
+//               waits for it (Y and Y_off are double-buffered in TMEM)
 // Every wait is bounded (clock64 budget); a timeout sets SSD_ERR_TIMEOUT in the workspace
 // status word, makes every role stop, drains in-flight copies and frees TMEM before exit.
 #include <cuda.h>
@@ -51,8 +53,9 @@ using namespace ptx;
 
 constexpr int kTile = 128;          // tokens per tile (MMA M)
 constexpr int kPS = 64;             // headdim columns per unit (MMA N of Y, Y_off, S)
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDt = 2, kWarpA = 3, kWarpB = 7;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDt = 2, kWarpC = 3;   // compute: warps 3..10
 constexpr int kThreads = 11 * 32;
+constexpr int kComputeThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTileBytes = kTile * 128;   // a 128-row x 128-byte swizzled tile (16 KB)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -76,8 +79,9 @@ struct Cfg {
     static constexpr int kNReg = NS / 64;             // 64-column regions of a B / C tile
     static constexpr int kXSt = NS == 128 ? 3 : 2;    // x / decay ring depth
     static constexpr int kBCStages = NS == 128 ? 2 : 1;
-    static constexpr int kGBuf = NS == 128 ? 2 : 1;   // G / P buffers in TMEM
+    static constexpr int kYBuf = NS == 128 ? 2 : 1;   // Y / Y_off accumulator buffers
     static constexpr int kMB = NS / 128;               // 128-row blocks of the state
+    static constexpr int kHReg = kMB * 32;             // state values per compute thread
     static constexpr uint32_t kBCBytes = 2 * kNReg * kTileBytes;
     // shared memory (byte offsets from a 1024-aligned base)
     static constexpr uint32_t kOffX = 0;
@@ -87,20 +91,21 @@ struct Cfg {
     static constexpr uint32_t kOffDt = kOffHt + NS * 128;
     static constexpr uint32_t kOffSmall = kOffDt + kXSt * sizeof(DtSlot);
     // TMEM columns
-    static constexpr uint32_t kColG = 0;
-    static constexpr uint32_t kColY = kGBuf * 128;
-    static constexpr uint32_t kColYoff = kColY + kPS;
-    static constexpr uint32_t kColS = kColYoff + kPS;
-    static constexpr uint32_t kColH = kColS + kMB * kPS;
-    static_assert(kColH + kMB * kPS <= kTmemCols, "TMEM budget");
+    static constexpr uint32_t kColG = 0;                       // C B^T, fp32, 128 columns
+    static constexpr uint32_t kColP = 128;                     // P, bf16 pairs, 64 columns
+    static constexpr uint32_t kColY = 192;                     // Y_diag, kYBuf x 64
+    static constexpr uint32_t kColYoff = kColY + kYBuf * kPS;  // Y_off, kYBuf x 64
+    static constexpr uint32_t kColS = kColYoff + kYBuf * kPS;  // S^T, kMB x 64
+    static_assert(kColS + kMB * kPS <= kTmemCols, "TMEM budget");
     static_assert(kXSt <= kXStagesMax, "x ring");
 };
 
 enum : int { kInitH0 = 0, kInitZero = 1, kInitLookback = 2 };
 enum : int { kFinNone = 0, kFinFinal = 1, kFinIncl = 2, kFinAgg = 3 };
 
+// Unit indices and coordinates fit in 32 bits (the launcher checks batch * H * P/64).
 struct Item {
-    int64_t u;        // unit
+    int u;            // unit
     int k0, k1;       // tile range of the unit's chain
     int pass1;        // 1: state-only pass (no y)
     int init;         // how the state starts: kInit*
@@ -116,7 +121,7 @@ struct Item {
 // the state a successor needs is published as early as possible and the state a range needs
 // is consumed as late as possible.
 struct Plan {
-    int64_t u0, u1, f_lo, n_full, n_items;
+    int u0, u1, f_lo, n_full, n_items;
     int k0, k1, n_pre, middle, p1;
 };
 
@@ -134,23 +139,23 @@ struct TcParams {
     __nv_bfloat16* y;
     float* hT;
     uint8_t* ws;
-    int* flags;         // per CTA and "B" warp: inclusive flag, aggregate flag, log2 decay
+    int* flags;         // per CTA and compute warp: inclusive flag, aggregate flag, log2 decay
     float* slots;       // per CTA: inclusive state [64 x N], then aggregate state [64 x N]
     long long budget;   // clock64 cycles a single wait may take
 };
 
 struct Small {
     uint64_t x_full[kXStagesMax], x_empty[kXStagesMax];   // x tile + decay slot
-    uint64_t bc_full[2], bc_empty[2];                // B / C tiles
-    uint64_t g_full[2], gp_empty[2];                 // G written / P read by Y_diag
-    // P is built by both warpgroups; each has its own barrier, because the "A" warpgroup may
-    // finish the next tile's half before the "B" warpgroup finishes this tile's half
-    uint64_t p_full_a, p_full_b;
-    uint64_t xt_full, xt_empty, s_full, s_empty, h_full, h_empty, y_full, y_empty;
+    uint64_t bc_full[2], bc_empty[2];                      // B / C tiles
+    uint64_t g_full, g_empty;       // C B^T written / read by the P builders
+    uint64_t p_full, p_empty;       // P written / read by Y_diag
+    uint64_t xt_full, xt_empty, s_full, s_empty, h_full, h_empty;
+    uint64_t y_full[2], y_empty[2];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
     Plan plan;
+    int uc_u0[6], uc_u1[6], uc_flo[6];   // coordinates of the plan's anchor units
 };
 
 __device__ __forceinline__ Plan make_plan(const TcParams& p, int cta) {
@@ -162,8 +167,8 @@ __device__ __forceinline__ Plan make_plan(const TcParams& p, int cta) {
     const int64_t start = (int64_t)cta * total / p.n_ctas;
     const int64_t end = (int64_t)(cta + 1) * total / p.n_ctas;
     if (start >= end) return pl;
-    pl.u0 = start / T;
-    pl.u1 = (end - 1) / T;
+    pl.u0 = (int)(start / T);
+    pl.u1 = (int)((end - 1) / T);
     pl.k0 = (int)(start % T);
     pl.k1 = (int)((end - 1) % T + 1);
     if (pl.u0 == pl.u1 && pl.k0 > 0 && pl.k1 < T) {     // middle piece of one chain
@@ -176,8 +181,8 @@ __device__ __forceinline__ Plan make_plan(const TcParams& p, int cta) {
     const bool head = (pl.u0 == pl.u1) ? (pl.k0 == 0 && pl.k1 < T) : (pl.k1 < T);
     const bool tail = pl.k0 > 0;
     pl.n_pre = head ? 1 + pl.p1 : 0;
-    const int64_t f_first = tail ? pl.u0 + 1 : pl.u0;
-    const int64_t f_last = head ? pl.u1 - 1 : pl.u1;
+    const int f_first = tail ? pl.u0 + 1 : pl.u0;
+    const int f_last = head ? pl.u1 - 1 : pl.u1;
     if (f_last >= f_first) {
         pl.f_lo = f_first;
         pl.n_full = f_last - f_first + 1;
@@ -186,7 +191,7 @@ __device__ __forceinline__ Plan make_plan(const TcParams& p, int cta) {
     return pl;
 }
 
-__device__ __forceinline__ Item plan_item(const Plan& pl, int64_t i, int T) {
+__device__ __forceinline__ Item plan_item(const Plan& pl, int i, int T) {
     if (pl.middle) {
         if (pl.n_pre > 0 && i == 0) return Item{pl.u0, pl.k0, pl.k1, 1, kInitZero, kFinAgg};
         return Item{pl.u0, pl.k0, pl.k1, 0, kInitLookback, kFinIncl};
@@ -201,41 +206,78 @@ __device__ __forceinline__ Item plan_item(const Plan& pl, int64_t i, int T) {
 }
 
 struct UnitCoords {
-    int64_t b, h, g, bh;
-    int ps;
+    int b, h, g, bh, ps;
+    int hr;             // h % (H / G): position of h inside its group
 };
 
-__device__ __forceinline__ UnitCoords unit_coords(const TcParams& p, int64_t u) {
+// Coordinates of unit u (divisions: computed once per CTA, for the plan's anchor units).
+__device__ __forceinline__ UnitCoords unit_coords(const TcParams& p, int u) {
+    const int H = (int)p.H, R = (int)(p.H / p.G);
     UnitCoords c;
-    c.ps = (int)(u % p.n_ps);
+    c.ps = u % p.n_ps;
     c.bh = u / p.n_ps;
-    c.h = c.bh % p.H;
-    c.b = c.bh / p.H;
-    c.g = c.h / (p.H / p.G);
+    c.h = c.bh % H;
+    c.b = c.bh / H;
+    c.g = c.h / R;
+    c.hr = c.h % R;
     return c;
+}
+
+// Coordinates of unit u + 1 from those of u (no divisions).
+__device__ __forceinline__ void next_unit(UnitCoords& c, const TcParams& p) {
+    if (++c.ps < p.n_ps) return;
+    c.ps = 0;
+    ++c.bh;
+    ++c.h;
+    if (++c.hr == (int)(p.H / p.G)) {
+        c.hr = 0;
+        ++c.g;
+    }
+    if (c.h == (int)p.H) {
+        c.h = 0;
+        c.g = 0;
+        c.hr = 0;
+        ++c.b;
+    }
 }
 
 // Position in a CTA's sequence of tiles; the unit's coordinates are refreshed only when the
 // item changes.
 struct Cursor {
-    int64_t item;
+    int item;
     int k;
     bool valid;
     Item it;
     UnitCoords uc;
 };
 
-__device__ __forceinline__ Cursor first_tile(const Plan& pl, const TcParams& p) {
+// Coordinates of an item's unit: one of the plan's anchors (u0, u1, f_lo), else the unit after
+// the previous item's (whole chains run in unit order).
+__device__ __forceinline__ void item_coords(Cursor& c, const Plan& pl, const Small& sm,
+                                            int prev_u, const TcParams& p) {
+    const int* a = c.it.u == pl.u0
+                       ? sm.uc_u0
+                       : (c.it.u == pl.u1 ? sm.uc_u1 : (c.it.u == pl.f_lo ? sm.uc_flo : nullptr));
+    if (a) {
+        c.uc = UnitCoords{a[0], a[1], a[2], a[3], a[4], a[5]};
+    } else if (c.it.u != prev_u) {
+        next_unit(c.uc, p);
+    }
+}
+
+__device__ __forceinline__ Cursor first_tile(const Plan& pl, const Small& sm, const TcParams& p) {
     Cursor c;
     c.item = 0;
     c.valid = pl.n_items > 0;
     c.it = plan_item(pl, 0, p.n_tiles);
     c.k = c.it.k0;
-    c.uc = unit_coords(p, c.valid ? c.it.u : 0);
+    c.uc = UnitCoords{0, 0, 0, 0, 0, 0};
+    item_coords(c, pl, sm, -1, p);
     return c;
 }
 
-__device__ __forceinline__ void advance(Cursor& c, const Plan& pl, const TcParams& p) {
+__device__ __forceinline__ void advance(Cursor& c, const Plan& pl, const Small& sm,
+                                        const TcParams& p) {
     if (!c.valid) return;
     if (c.k + 1 < c.it.k1) {
         ++c.k;
@@ -244,9 +286,10 @@ __device__ __forceinline__ void advance(Cursor& c, const Plan& pl, const TcParam
     ++c.item;
     c.valid = c.item < pl.n_items;
     if (c.valid) {
+        const int prev_u = c.it.u;
         c.it = plan_item(pl, c.item, p.n_tiles);
         c.k = c.it.k0;
-        c.uc = unit_coords(p, c.it.u);
+        item_coords(c, pl, sm, prev_u, p);
     }
 }
 
@@ -258,16 +301,18 @@ __device__ __forceinline__ void flag_abort(Small& sm, uint8_t* ws) {
 // Bounded wait for the completion of the phase with `parity`.  False on timeout or abort.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Small& sm,
                                          const TcParams& p) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+    long long t0 = -1;
+    while (!mbar_try_wait(bar, parity)) {
         if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) return false;
-        if (clock64() - t0 > p.budget) {
+        const long long t = clock64();
+        if (t0 < 0) {
+            t0 = t;
+        } else if (t - t0 > p.budget) {
             flag_abort(sm, p.ws);
             return false;
         }
     }
+    return true;
 }
 
 // wait_bar for the 32 lanes of a warp, with one verdict for the whole warp, so the warp stays
@@ -277,136 +322,110 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Small&
     return __all_sync(0xffffffffu, wait_bar(bar, parity, sm, p));
 }
 
-// One 32 x 32 block (rows 32q .. 32q+31, columns 32jb .. 32jb+31) of P = L o G o dt_j.
-// Reads G's block from TMEM and writes P's block (bf16 pairs) into the upper 16 columns of the
-// same 32 columns, which only this thread's lane ever reads, so the overwrite is race-free.
-// Above the diagonal the block is zero; strictly below it every L_ij factors exactly as
-// exp(cum_i - m) exp(m - cum_j) with m = cum at row 32q - 1 (between cum_i and cum_j), so the
-// block needs no exponential; the diagonal block is masked before the exponential.
-__device__ __forceinline__ void p_block(uint32_t tg, int jb, int q, int lane, int r,
-                                        const DtSlot& sl) {
-    uint32_t pk[16];
-    if (jb > q) {
+// One 32 x 32 block (rows 32q .. 32q+31, columns 32jb .. 32jb+31) of P = L o G o dt_j for this
+// lane's row: G's block is read from TMEM (tg) and the bf16 pairs are returned in pk.  Strictly
+// below the diagonal block every L_ij factors exactly as exp(cum_i - m) exp(m - cum_j) with
+// m = cum at row 32q - 1 (between cum_i and cum_j), so the block needs no exponential; the
+// diagonal block is masked before the exponential.  (Blocks above the diagonal are zero and
+// are written once, at kernel start.)
+__device__ __forceinline__ void p_block(uint32_t (&pk)[16], uint32_t tg, int jb, int q, int lane,
+                                        int r, const DtSlot& sl) {
+    float g[32];
+    tmem_ld32(tg, g);
+    if (jb < q) {
+        const float ur = sl.urow[r];
+        const float4* cf = reinterpret_cast<const float4*>(&sl.colf[q - 1][jb * 32]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+        for (int i = 0; i < 8; ++i) {
+            const float4 c = cf[i];
+            g[4 * i + 0] *= c.x * ur;
+            g[4 * i + 1] *= c.y * ur;
+            g[4 * i + 2] *= c.z * ur;
+            g[4 * i + 3] *= c.w * ur;
+        }
     } else {
-        float g[32];
-        tmem_ld32(tg, g);
-        if (jb < q) {
-            const float ur = sl.urow[r];
-            const float4* cf = reinterpret_cast<const float4*>(&sl.colf[q - 1][jb * 32]);
+        const float c2 = sl.cum2[r];
+        const float4* pc = reinterpret_cast<const float4*>(&sl.pcol[jb * 32]);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 c = cf[i];
-                g[4 * i + 0] *= c.x * ur;
-                g[4 * i + 1] *= c.y * ur;
-                g[4 * i + 2] *= c.z * ur;
-                g[4 * i + 3] *= c.w * ur;
-            }
-        } else {
-            const float c2 = sl.cum2[r];
-            const float4* pc = reinterpret_cast<const float4*>(&sl.pcol[jb * 32]);
+        for (int i = 0; i < 8; ++i) {
+            const float4 c = pc[i];
+            const float cv[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 c = pc[i];
-                const float cv[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int jj = 4 * i + e;
-                    g[jj] = (jj <= lane) ? ex2(c2 - cv[e]) * g[jj] : 0.f;
-                }
+            for (int e = 0; e < 4; ++e) {
+                const int jj = 4 * i + e;
+                g[jj] = (jj <= lane) ? ex2(c2 - cv[e]) * g[jj] : 0.f;
             }
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(g[2 * i], g[2 * i + 1]);
     }
-    tmem_st16(tg + 16, pk);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(g[2 * i], g[2 * i + 1]);
 }
 
-// ---- the state h^T in TMEM (this thread's lane; th = lane base + first state column) ----------
-// Columns: 32-column block cb = 2 mb + half holds state rows n = 128 mb + r, columns
-// p = 32 half .. 32 half + 31.
+// ---- the state in registers of the compute threads -------------------------------------------
+// Compute thread (row r, column half c0) holds h^T rows n = 128 mb + r, columns p = c0 .. c0+31.
 
-// H <- scale * src + H when `accumulate`, else H <- src.  src is a [64 x N] fp32 block (element
+// h <- scale * src + h when `accumulate`, else h <- src.  src is a [64 x N] fp32 block (element
 // (p, n) at p * ld + n); nullptr means zeros.  `l2only` reads bypass L1 (for states another SM
 // published).
 template <int NS>
-__device__ __forceinline__ void state_from(uint32_t th, int r, const float* src, int64_t ld,
-                                           float scale, bool accumulate, bool l2only) {
-#pragma unroll 1
-    for (int cb = 0; cb < NS / 64; ++cb) {
-        const int n = (cb >> 1) * 128 + r, half = cb & 1;
-        float v[32];
-        if (accumulate) tmem_ld32(th + cb * 32, v);
+__device__ __forceinline__ void h_from(float (&h)[NS / 4], const float* src, int64_t ld, int r,
+                                       int c0, float scale, bool accumulate, bool l2only) {
+#pragma unroll
+    for (int mb = 0; mb < NS / 128; ++mb)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             float x = 0.f;
             if (src) {
-                const float* a = src + (int64_t)(half * 32 + i) * ld + n;
+                const float* a = src + (int64_t)(c0 + i) * ld + mb * 128 + r;
                 x = l2only ? __ldcg(a) : *a;
             }
-            v[i] = accumulate ? fmaf(scale, x, v[i]) : x;
+            h[mb * 32 + i] = accumulate ? fmaf(scale, x, h[mb * 32 + i]) : x;
         }
-        tmem_st32(th + cb * 32, v);
-    }
 }
 
-// dst[p][n] <- H (fp32)
+// dst[p][n] <- h (fp32)
 template <int NS>
-__device__ __forceinline__ void state_to(uint32_t th, int r, float* dst, int64_t ld) {
-#pragma unroll 1
-    for (int cb = 0; cb < NS / 64; ++cb) {
-        const int n = (cb >> 1) * 128 + r, half = cb & 1;
-        float v[32];
-        tmem_ld32(th + cb * 32, v);
+__device__ __forceinline__ void h_to(const float (&h)[NS / 4], float* dst, int64_t ld, int r,
+                                     int c0) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dst[(int64_t)(half * 32 + i) * ld + n] = v[i];
-    }
+    for (int mb = 0; mb < NS / 128; ++mb)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dst[(int64_t)(c0 + i) * ld + mb * 128 + r] = h[mb * 32 + i];
 }
 
-// h^T (bf16, MN-major 128-byte swizzled tile of N rows x 64 columns at shared address ht) <- H,
-// the B operand of the next off-diagonal GEMM.
+// bf16 h^T into the MN-major, 128-byte swizzled tile (N rows x 64 columns) at ht: the B operand
+// of the next off-diagonal GEMM.
 template <int NS>
-__device__ __forceinline__ void ht_from_state(uint32_t th, int r, uint32_t ht) {
-#pragma unroll 1
-    for (int cb = 0; cb < NS / 64; ++cb) {
-        const int n = (cb >> 1) * 128 + r, half = cb & 1;
-        float v[32];
-        tmem_ld32(th + cb * 32, v);
+__device__ __forceinline__ void ht_write(const float (&h)[NS / 4], uint8_t* ht, int r, int hsel) {
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-            st_shared_v4(ht + sw128_off(n, half * 4 + cc), pack_bf16x2(v[cc * 8 + 0], v[cc * 8 + 1]),
-                         pack_bf16x2(v[cc * 8 + 2], v[cc * 8 + 3]),
-                         pack_bf16x2(v[cc * 8 + 4], v[cc * 8 + 5]),
-                         pack_bf16x2(v[cc * 8 + 6], v[cc * 8 + 7]));
-    }
-    fence_proxy_async_smem();
+    for (int mb = 0; mb < NS / 128; ++mb)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const float* v = &h[mb * 32 + cc * 8];
+            *reinterpret_cast<uint4*>(ht + sw128_off(mb * 128 + r, hsel * 4 + cc)) =
+                make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                           pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+        }
 }
 
-// Flags of the state hand-off between CTAs, per CTA and per "B" warp q (the warp that owns
-// state rows 32q .. 32q+31 of every 128-row block): [0] inclusive state published,
-// [1] aggregate published, [2] the aggregate's log2 decay.  A warp only needs the same rows of
-// its predecessor, so publishing and looking back are per warp, with no warpgroup barrier.
-constexpr int kFlagsPerCta = 16;
+// Flags of the state hand-off between CTAs, per CTA and per compute warp w (the warp that owns
+// state rows 32q .. 32q+31 of every 128-row block and one column half): [0] inclusive state
+// published, [1] aggregate published, [2] the aggregate's log2 decay.  A warp only needs the
+// same part of its predecessor's state, so publishing and looking back are per warp.
+constexpr int kFlagsPerCta = 32;
 
-// The state entering an item's first tile (per "B" warp; out of line, as it runs a few times
-// per CTA).  kInitZero: zeros; kInitH0: h0 (or zeros); kInitLookback: a decoupled look-back
-// over the preceding ranges' published states,
+// Decoupled look-back over the preceding ranges' published states (per compute warp):
 //     h_in = D_1 (D_2 (... h_incl ...) + H_2) + H_1.
-// Returns false on timeout or abort.
+// False on timeout or abort.
 template <int NS>
-__device__ __noinline__ bool state_begin(const TcParams& p, Small& sm, uint32_t th, int q,
-                                         int lane, int init, const float* h0) {
-    const int r = q * 32 + lane;
-    if (init != kInitLookback) {
-        state_from<NS>(th, r, init == kInitH0 ? h0 : nullptr, p.N, 0.f, false, false);
-        return true;
-    }
+__device__ __forceinline__ bool look_back(float (&h)[NS / 4], const TcParams& p, Small& sm,
+                                          int w, int lane, int r, int c0) {
     const int64_t slot_elems = (int64_t)kPS * NS;
-    state_from<NS>(th, r, nullptr, p.N, 0.f, false, false);
+    h_from<NS>(h, nullptr, NS, r, c0, 0.f, false, false);
     float acc_logd = 0.f;
+#pragma unroll 1
     for (int jp = (int)blockIdx.x - 1; jp >= 0; --jp) {
-        const int* f = p.flags + jp * kFlagsPerCta + q * 4;
+        const int* f = p.flags + jp * kFlagsPerCta + w * 4;
         int kind = 0;
         if (lane == 0) {
             const long long t0 = clock64();
@@ -422,38 +441,41 @@ __device__ __noinline__ bool state_begin(const TcParams& p, Small& sm, uint32_t 
         }
         kind = __shfl_sync(0xffffffffu, kind, 0);
         if (kind == 0) return false;
-        // every lane acquires the flag itself before it reads the published rows
+        // every lane acquires the flag itself before it reads the published state
         (void)ld_acquire_gpu(f + kind - 1);
-        const float* slot = p.slots + (int64_t)jp * 2 * slot_elems;
-        state_from<NS>(th, r, kind == 1 ? slot : slot + slot_elems, NS, ex2(acc_logd), true,
-                       true);
+        const float* slot = p.slots + (int64_t)jp * 2 * slot_elems + (kind == 2 ? slot_elems : 0);
+        h_from<NS>(h, slot, NS, r, c0, ex2(acc_logd), true, true);
         if (kind == 1) return true;
         acc_logd += __int_as_float(__ldcg(f + 2));
     }
     return false;   // no inclusive state before this range: cannot happen for a valid plan
 }
 
-// The end of an item (per "B" warp, out of line): the final state into dst (kFinFinal, dst
-// may be null), or this CTA's inclusive state / aggregate published for the next range
-// (kFinIncl / kFinAgg, dst = the slot).
+// This warp's part of the CTA's inclusive state (kFinIncl) or aggregate (kFinAgg), published
+// for the next range.
 template <int NS>
-__device__ __noinline__ void state_end(const TcParams& p, uint32_t th, int q, int lane, int fin,
-                                       float* dst, float item_logd) {
-    const int r = q * 32 + lane;
-    if (fin == kFinFinal) {
-        if (dst) state_to<NS>(th, r, dst, p.N);
-        return;
-    }
-    state_to<NS>(th, r, dst, NS);
+__device__ __forceinline__ void publish(const float (&h)[NS / 4], const TcParams& p, int w,
+                                        int lane, int r, int c0, int fin, float item_logd) {
+    const int64_t slot_elems = (int64_t)kPS * NS;
+    float* slot = p.slots + (int64_t)blockIdx.x * 2 * slot_elems + (fin == kFinAgg ? slot_elems : 0);
+    h_to<NS>(h, slot, NS, r, c0);
     __threadfence();
     __syncwarp();
     if (lane == 0) {
-        int* f = p.flags + (int)blockIdx.x * kFlagsPerCta + q * 4;
+        int* f = p.flags + (int)blockIdx.x * kFlagsPerCta + w * 4;
         if (fin == kFinAgg) st_relaxed_gpu(f + 2, __float_as_int(item_logd));
         st_release_gpu(f + (fin == kFinAgg ? 1 : 0), 1);
     }
     __syncwarp();
 }
+
+// A tile whose y epilogue is deferred by one tile (always the previous full tile).
+struct PendingY {
+    __nv_bfloat16* row;     // y row at this thread's column half, or null past the sequence end
+    float e;                // exp(cum) of the row
+    float d;                // D of the head
+    uint4 x[4];             // x row, this thread's column half (bf16 pairs)
+};
 
 template <int NS>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -473,27 +495,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < K::kXSt; ++i) {
             mbar_init(&sm.x_full[i], 1 + 32);
-            mbar_init(&sm.x_empty[i], 1 + 128);
+            mbar_init(&sm.x_empty[i], 1 + kComputeThreads);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.bc_full[i], 1);
             mbar_init(&sm.bc_empty[i], 1);
-            mbar_init(&sm.g_full[i], 1);
-            mbar_init(&sm.gp_empty[i], 1);
+            mbar_init(&sm.y_full[i], 1);
+            mbar_init(&sm.y_empty[i], kComputeThreads);
         }
-        mbar_init(&sm.xt_full, 128);
+        mbar_init(&sm.g_full, 1);
+        mbar_init(&sm.g_empty, kComputeThreads);
+        mbar_init(&sm.p_full, kComputeThreads);
+        mbar_init(&sm.p_empty, 1);
+        mbar_init(&sm.xt_full, kComputeThreads);
         mbar_init(&sm.xt_empty, 1);
-        mbar_init(&sm.p_full_a, 128);
-        mbar_init(&sm.p_full_b, 128);
         mbar_init(&sm.s_full, 1);
-        mbar_init(&sm.s_empty, 128);
-        mbar_init(&sm.h_full, 128);
+        mbar_init(&sm.s_empty, kComputeThreads);
+        mbar_init(&sm.h_full, kComputeThreads);
         mbar_init(&sm.h_empty, 1);
-        mbar_init(&sm.y_full, 1);
-        mbar_init(&sm.y_empty, 128);
         mbar_init(&sm.mma_done, 1);
         sm.abort_flag = 0;
         sm.plan = make_plan(p, blockIdx.x);
+        const int us[3] = {sm.plan.u0, sm.plan.u1, sm.plan.f_lo};
+        int* dst[3] = {sm.uc_u0, sm.uc_u1, sm.uc_flo};
+        for (int i = 0; i < 3; ++i) {
+            const UnitCoords c = unit_coords(p, us[i]);
+            dst[i][0] = c.b;
+            dst[i][1] = c.h;
+            dst[i][2] = c.g;
+            dst[i][3] = c.bh;
+            dst[i][4] = c.ps;
+            dst[i][5] = c.hr;
+        }
         fence_mbar_init();
     }
     if (warp == kWarpMma) {
@@ -511,25 +544,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sm.tmem_base;
     const Plan& plan = sm.plan;
 
+    // P's blocks above the diagonal are zero in every tile: written once
+    if (warp >= kWarpC) {
+        const int q = warp & 3, hsel = (warp - kWarpC) >> 2;
+        const uint32_t tp = tmem + ((uint32_t)(q * 32) << 16) + K::kColP;
+        uint32_t z[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) z[i] = 0u;
+        const int jbA = hsel ? 1 : 0, jbB = hsel ? 2 : 3;
+        if (jbA > q) tmem_st16(tp + 16 * jbA, z);
+        if (jbB > q) tmem_st16(tp + 16 * jbB, z);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
     if (warp == kWarpTma) {
         // ------------------------------------------------------- B / C TMA producer ----
         if (lane == 0) {
             int nt = 0;
-            for (Cursor c = first_tile(plan, p); c.valid; advance(c, plan, p), ++nt) {
+            for (Cursor c = first_tile(plan, sm, p); c.valid; advance(c, plan, sm, p), ++nt) {
                 const int s = nt % K::kBCStages;
                 const uint32_t use = nt / K::kBCStages;
                 if (!wait_bar(&sm.bc_empty[s], (use & 1u) ^ 1u, sm, p)) break;
                 const int t0 = c.k * kTile;
-                const int g = (int)c.uc.g, b = (int)c.uc.b;
                 // a state-only tile needs B; a full tile also C
                 mbar_arrive_expect_tx(&sm.bc_full[s],
                                       (c.it.pass1 ? 1 : 2) * K::kNReg * kTileBytes);
                 uint8_t* dst = smem + K::kOffBC + s * K::kBCBytes;
                 for (int r = 0; r < K::kNReg; ++r) {
-                    tma_load_4d(dst + r * kTileBytes, &tmB, &sm.bc_full[s], r * 64, g, t0, b);
+                    tma_load_4d(dst + r * kTileBytes, &tmB, &sm.bc_full[s], r * 64, c.uc.g, t0,
+                                c.uc.b);
                     if (!c.it.pass1)
                         tma_load_4d(dst + (K::kNReg + r) * kTileBytes, &tmC, &sm.bc_full[s],
-                                    r * 64, g, t0, b);
+                                    r * 64, c.uc.g, t0, c.uc.b);
                 }
             }
             if (sm.abort_flag) {
@@ -547,42 +596,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kWarpDt) {
         // ------------------------------------------ x TMA + decay-factor producer ----
-        // dt of the tile two ahead is loaded into registers while this tile is computed.
-        auto load_dt = [&](const Cursor& c, float (&v)[4]) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = 0.f;
-            if (!c.valid) return;
-            const int64_t t = (int64_t)c.k * kTile + 4 * lane;
-            const __nv_bfloat16* src = p.dt + (c.uc.b * p.L + t) * p.H + c.uc.h;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (t + i < p.L) v[i] = __bfloat162float(src[(int64_t)i * p.H]);
-        };
-        Cursor c = first_tile(plan, p);
-        Cursor cl = c;
-        float d0[4], d1[4];
-        load_dt(cl, d0);
-        advance(cl, plan, p);
-        load_dt(cl, d1);
-        advance(cl, plan, p);
         int nt = 0;
-        int64_t a_u = -1;
+        int a_u = -1;
         float A2 = 0.f;
-        for (; c.valid; advance(c, plan, p), ++nt) {
-            float d2[4];
-            load_dt(cl, d2);
-            advance(cl, plan, p);
+        for (Cursor c = first_tile(plan, sm, p); c.valid; advance(c, plan, sm, p), ++nt) {
+            // dt of this tile (4 consecutive tokens per lane): in flight during the wait below
+            float d0[4];
+            {
+                const int64_t t = (int64_t)c.k * kTile + 4 * lane;
+                const __nv_bfloat16* src = p.dt + ((int64_t)c.uc.b * p.L + t) * p.H + c.uc.h;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    d0[i] = t + i < p.L ? __bfloat162float(src[(int64_t)i * p.H]) : 0.f;
+            }
+            if (c.it.u != a_u) {
+                a_u = c.it.u;
+                A2 = p.A[c.uc.h] * kLog2e;
+            }
             const int s = nt % K::kXSt;
             const uint32_t use = nt / K::kXSt;
             if (!wait_warp(&sm.x_empty[s], (use & 1u) ^ 1u, sm, p)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&sm.x_full[s], kTileBytes);
                 tma_load_4d(smem + K::kOffX + s * kTileBytes, &tmX, &sm.x_full[s],
-                            c.uc.ps * kPS, (int)c.uc.h, c.k * kTile, (int)c.uc.b);
-            }
-            if (c.it.u != a_u) {
-                a_u = c.it.u;
-                A2 = p.A[c.uc.h] * kLog2e;
+                            c.uc.ps * kPS, c.uc.h, c.k * kTile, c.uc.b);
             }
             // log2-domain cumsum: 4 consecutive tokens per lane, then a warp scan
             float cs[4];
@@ -632,11 +669,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float4(v_f3[0], v_f3[1], v_f3[2], v_f3[3]);
             if (lane == 0) sl.clast2 = clast2;
             mbar_arrive(&sm.x_full[s]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                d0[i] = d1[i];
-                d1[i] = d2[i];
-            }
         }
         if (sm.abort_flag && lane == 0) {
             // drain: the x loads of every tile this loop completed must land before exit
@@ -656,37 +688,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS = idesc_bf16(128, kPS, 1, 1);
             constexpr uint32_t idYoff = idesc_bf16(128, kPS, 0, 1);
             constexpr uint32_t idYd = idesc_bf16(128, kPS, 0, 1);
-            // G = C B^T of tile number nt (the j-th full tile) into G buffer j % kGBuf
+            // G = C B^T of tile number nt (the j-th full tile), once the P builders have read
+            // the previous G
             auto issue_G = [&](int nt, int j) -> bool {
                 const int s = nt % K::kBCStages;
-                const int gb = j % K::kGBuf;
                 if (!wait_bar(&sm.bc_full[s], (uint32_t)(nt / K::kBCStages) & 1u, sm, p))
                     return false;
-                if (!wait_bar(&sm.gp_empty[gb], ((uint32_t)(j / K::kGBuf) & 1u) ^ 1u, sm, p))
-                    return false;
+                if (!wait_bar(&sm.g_empty, ((uint32_t)j & 1u) ^ 1u, sm, p)) return false;
                 tc_fence_after();
                 const uint32_t bbase = sbase + K::kOffBC + s * K::kBCBytes;
                 const uint32_t cbase = bbase + K::kNReg * kTileBytes;
 #pragma unroll 1
                 for (int kk = 0; kk < NS / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-                    mma_f16(tmem + K::kColG + gb * 128, smem_desc_sw128(cbase + off, 16, 1024),
+                    mma_f16(tmem + K::kColG, smem_desc_sw128(cbase + off, 16, 1024),
                             smem_desc_sw128(bbase + off, 16, 1024), idG, kk > 0);
                 }
-                mma_commit(&sm.g_full[gb]);
+                mma_commit(&sm.g_full);
                 return true;
             };
             int nt = 0, j = 0;           // tiles issued, full (non state-only) tiles issued
             bool g_ahead = false;        // G of the current tile was issued one tile early
-            Cursor c = first_tile(plan, p);
+            Cursor c = first_tile(plan, sm, p);
             for (; c.valid; ++nt) {
-                Cursor nx = c;
-                advance(nx, plan, p);
                 const int s = nt % K::kBCStages;
                 const int xs = nt % K::kXSt;
                 const uint32_t par = (uint32_t)nt & 1u;
                 const bool full_tile = !c.it.pass1;
-                const bool next_full = nx.valid && !nx.it.pass1;
+                const bool next_full =
+                    (c.k + 1 < c.it.k1)
+                        ? !c.it.pass1
+                        : (c.item + 1 < plan.n_items &&
+                           !plan_item(plan, c.item + 1, p.n_tiles).pass1);
                 if (full_tile && !g_ahead && !issue_G(nt, j)) break;
                 g_ahead = false;
                 // chunk state S^T = B^T (w o X)
@@ -713,13 +746,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!full_tile) {
                     mma_commit(&sm.bc_empty[s]);
                     mma_commit(&sm.x_empty[xs]);
-                    c = nx;
+                    advance(c, plan, sm, p);
                     continue;
                 }
-                const uint32_t jpar = (uint32_t)j & 1u;
-                const int gb = j % K::kGBuf;
-                // off-diagonal Y_off = C h_prev^T
-                if (!wait_bar(&sm.h_full, jpar, sm, p) || !wait_bar(&sm.y_empty, jpar ^ 1u, sm, p))
+                const int yb = j % K::kYBuf;
+                const uint32_t ypar = (uint32_t)(j / K::kYBuf) & 1u;
+                // off-diagonal Y_off = C h_prev^T, into the accumulator buffer of this tile
+                if (!wait_bar(&sm.h_full, (uint32_t)j & 1u, sm, p) ||
+                    !wait_bar(&sm.y_empty[yb], ypar ^ 1u, sm, p))
                     break;
                 tc_fence_after();
                 {
@@ -728,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t ht = sbase + K::kOffHt;
 #pragma unroll 1
                     for (int kk = 0; kk < NS / 16; ++kk)
-                        mma_f16(tmem + K::kColYoff,
+                        mma_f16(tmem + K::kColYoff + yb * kPS,
                                 smem_desc_sw128(cbase + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16,
                                                 1024),
                                 smem_desc_sw128(ht + kk * 2048, 1024, 1024), idYoff, kk > 0);
@@ -740,27 +774,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!issue_G(nt + 1, j + 1)) break;
                     g_ahead = true;
                 }
-                // Y_diag = P X, P read from TMEM (upper 16 of each 32 G columns)
-                if (!wait_bar(&sm.p_full_a, jpar, sm, p) || !wait_bar(&sm.p_full_b, jpar, sm, p))
-                    break;
+                // Y_diag = P X, P read from TMEM
+                if (!wait_bar(&sm.p_full, (uint32_t)j & 1u, sm, p)) break;
                 tc_fence_after();
                 {
-                    const uint32_t pcol = tmem + K::kColG + gb * 128 + 16;
                     const uint32_t xb = sbase + K::kOffX + xs * kTileBytes;
 #pragma unroll 1
                     for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_f16_ts(tmem + K::kColY, pcol + (kk >> 1) * 32 + (kk & 1) * 8,
+                        mma_f16_ts(tmem + K::kColY + yb * kPS, tmem + K::kColP + kk * 8,
                                    smem_desc_sw128(xb + kk * 2048, 1024, 1024), idYd, kk > 0);
                 }
-                mma_commit(&sm.y_full);
-                mma_commit(&sm.gp_empty[gb]);
+                mma_commit(&sm.y_full[yb]);
+                mma_commit(&sm.p_empty);
                 mma_commit(&sm.x_empty[xs]);
                 if (K::kBCStages == 1 && next_full) {
                     if (!issue_G(nt + 1, j + 1)) break;
                     g_ahead = true;
                 }
                 ++j;
-                c = nx;
+                advance(c, plan, sm, p);
             }
             // every MMA issued above has completed once this barrier's phase 0 completes
             mma_commit(&sm.mma_done);
@@ -768,181 +800,202 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (!mbar_try_wait(&sm.mma_done, 0) && clock64() - t0 < p.budget) {
             }
         }
-    } else if (warp < kWarpB) {
-        // ---------------------------------------------------------------- "A" warpgroup ---
-        const int q = warp & 3;                 // TMEM lane quarter
-        const int r = q * 32 + lane;            // tile row
+    } else {
+        // ------------------------------------------------------------- compute warps -----
+        const int w = warp - kWarpC;             // 0..7
+        const int q = warp & 3;                  // TMEM lane quarter
+        const int hsel = w >> 2;                 // column half
+        const int r = q * 32 + lane;             // tile row, and state row inside a 128-block
+        const int c0 = hsel * 32;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        int nt = 0, j = 0;
-        for (Cursor c = first_tile(plan, p); c.valid; advance(c, plan, p), ++nt) {
-            const int xs = nt % K::kXSt;
-            const uint32_t par = (uint32_t)nt & 1u;
-            const bool full_tile = !c.it.pass1;
-            if (!wait_warp(&sm.x_full[xs], (uint32_t)(nt / K::kXSt) & 1u, sm, p)) break;
-            const DtSlot& sl = slots[xs];
-            // w o X for the chunk-state GEMM: row r scaled by exp(cum_last - cum_r) dt_r
-            if (!wait_warp(&sm.xt_empty, par ^ 1u, sm, p)) break;
-            {
-                const float wr = sl.w[r];
-                const uint32_t xrow = sbase + K::kOffX + xs * kTileBytes;
-                const uint32_t xtrow = sbase + K::kOffXt;
+        // P column blocks of this warpgroup, balanced over the lane quarters
+        const int jbA = hsel ? 1 : 0, jbB = hsel ? 2 : 3;
+        float h[K::kHReg];
+        PendingY pend;
+        bool have_pend = false;
+        // the deferred y epilogue of full tile pj: y = Y_diag + exp(cum) Y_off + D x for this
+        // thread's half row, in two 16-column steps
+        auto epilogue = [&](int pj) -> bool {
+            const int yb = pj % K::kYBuf;
+            if (!wait_warp(&sm.y_full[yb], (uint32_t)(pj / K::kYBuf) & 1u, sm, p)) return false;
+            tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint32_t off = sw128_off(r, cc);
-                    const uint4 v = ld_shared_v4(xrow + off);
-                    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+            for (int qc = 0; qc < 2; ++qc) {
+                float yd[16], yo[16];
+                tmem_ld16x2(tmem + lane_base + K::kColY + yb * kPS + c0 + qc * 16, yd,
+                            tmem + lane_base + K::kColYoff + yb * kPS + c0 + qc * 16, yo);
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const uint4 xv = pend.x[qc * 2 + cc];
+                    const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
                     uint32_t o[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        o[e] = pack_bf16x2(wr * bf16lo_to_f32(in[e]), wr * bf16hi_to_f32(in[e]));
-                    st_shared_v4(xtrow + off, o[0], o[1], o[2], o[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const int i0 = cc * 8 + e * 2;
+                        const float v0 =
+                            fmaf(pend.d, bf16lo_to_f32(xin[e]), fmaf(pend.e, yo[i0], yd[i0]));
+                        const float v1 = fmaf(pend.d, bf16hi_to_f32(xin[e]),
+                                              fmaf(pend.e, yo[i0 + 1], yd[i0 + 1]));
+                        o[e] = pack_bf16x2(v0, v1);
+                    }
+                    if (pend.row)
+                        *reinterpret_cast<uint4*>(pend.row + qc * 16 + cc * 8) =
+                            make_uint4(o[0], o[1], o[2], o[3]);
                 }
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&sm.xt_full);
-            if (full_tile) {
-                // column blocks 0 and 1 of P (the "B" warpgroup builds blocks 2 and 3)
-                const int gb = j % K::kGBuf;
-                if (!wait_warp(&sm.g_full[gb], (uint32_t)(j / K::kGBuf) & 1u, sm, p)) break;
-                tc_fence_after();
-                const uint32_t tg = tmem + lane_base + K::kColG + gb * 128;
-#pragma unroll 1
-                for (int jb = 0; jb < 2; ++jb) p_block(tg + jb * 32, jb, q, lane, r, sl);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&sm.p_full_a);
-                ++j;
-            }
-        }
-    } else {
-        // ---------------------------------------------------------------- "B" warpgroup ---
-        // The state h^T (rows n = 128 mb + r, columns p) lives in TMEM columns kColH + 64 mb.
-        const int q = warp & 3;
-        const int r = q * 32 + lane;             // tile row, and state row inside a 128-block
-        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        const uint32_t th = tmem + lane_base + K::kColH;
+            tc_fence_before();
+            mbar_arrive(&sm.y_empty[yb]);
+            return true;
+        };
         int nt = 0, j = 0;
-        int64_t b_u = -1;
+        int d_u = -1;
         float Dh = 0.f;
         float item_logd = 0.f;                   // sum of log2 tile decays over the item
-        Cursor c = first_tile(plan, p);
-        for (; c.valid; ++nt) {
-            Cursor nx = c;
-            advance(nx, plan, p);
+        bool ok = true;
+        for (Cursor c = first_tile(plan, sm, p); c.valid; advance(c, plan, sm, p), ++nt) {
             const UnitCoords& uc = c.uc;
             const bool full_tile = !c.it.pass1;
             const int xs = nt % K::kXSt;
             const uint32_t par = (uint32_t)nt & 1u;
+            const bool last_of_item = c.k + 1 == c.it.k1;
             if (c.k == c.it.k0) {
-                // ---- start of an item: the state entering its first tile
+                // ---- start of an item: flush the deferred epilogue, then the entering state
+                if (have_pend) {
+                    if (!epilogue(j - 1)) { ok = false; break; }
+                    have_pend = false;
+                }
                 item_logd = 0.f;
-                if (c.it.u != b_u) {
-                    b_u = c.it.u;
+                if (c.it.u != d_u) {
+                    d_u = c.it.u;
                     Dh = p.D ? p.D[uc.h] : 0.f;
                 }
-                const int64_t hbase = (uc.bh * p.P + (int64_t)uc.ps * kPS) * p.N;
-                if (!state_begin<NS>(p, sm, th, q, lane, c.it.init,
-                                     p.h0 ? p.h0 + hbase : nullptr))
-                    break;
+                if (c.it.init == kInitLookback) {
+                    if (!look_back<NS>(h, p, sm, w, lane, r, c0)) { ok = false; break; }
+                } else {
+                    const float* src = (c.it.init == kInitH0 && p.h0)
+                                           ? p.h0 + ((int64_t)uc.bh * p.P + (int64_t)uc.ps * kPS) * p.N
+                                           : nullptr;
+                    h_from<NS>(h, src, p.N, r, c0, 0.f, false, false);
+                }
                 if (full_tile) {
                     // h^T for the item's first Y_off, once the previous full tile's Y_off is done
-                    if (j > 0 && !wait_warp(&sm.h_empty, (uint32_t)(j - 1) & 1u, sm, p)) break;
-                    ht_from_state<NS>(th, r, sbase + K::kOffHt);
+                    if (j > 0 && !wait_warp(&sm.h_empty, (uint32_t)(j - 1) & 1u, sm, p)) {
+                        ok = false;
+                        break;
+                    }
+                    ht_write<NS>(h, smem + K::kOffHt, r, hsel);
+                    fence_proxy_async_smem();
                     mbar_arrive(&sm.h_full);
                 }
             }
-            if (!wait_warp(&sm.x_full[xs], (uint32_t)(nt / K::kXSt) & 1u, sm, p)) break;
+            if (!wait_warp(&sm.x_full[xs], (uint32_t)(nt / K::kXSt) & 1u, sm, p)) { ok = false; break; }
             const DtSlot& sl = slots[xs];
+
+            // w o X for the chunk-state GEMM: row r scaled by exp(cum_last - cum_r) dt_r; the raw
+            // x row stays in registers for this tile's (deferred) D x term
+            if (!wait_warp(&sm.xt_empty, par ^ 1u, sm, p)) { ok = false; break; }
+            uint4 xk[4];
+            {
+                const float wr = sl.w[r];
+                const uint8_t* xrow = smem + K::kOffX + xs * kTileBytes;
+                uint8_t* xtrow = smem + K::kOffXt;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    xk[cc] = *reinterpret_cast<const uint4*>(xrow + sw128_off(r, hsel * 4 + cc));
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint32_t in[4] = {xk[cc].x, xk[cc].y, xk[cc].z, xk[cc].w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        o[e] = pack_bf16x2(wr * bf16lo_to_f32(in[e]), wr * bf16hi_to_f32(in[e]));
+                    *reinterpret_cast<uint4*>(xtrow + sw128_off(r, hsel * 4 + cc)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&sm.xt_full);
+
+            if (full_tile) {
+                // this warp's two column blocks of P (those above the diagonal stay zero)
+                if (!wait_warp(&sm.g_full, (uint32_t)j & 1u, sm, p)) { ok = false; break; }
+                if (!wait_warp(&sm.p_empty, ((uint32_t)j & 1u) ^ 1u, sm, p)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t tg = tmem + lane_base + K::kColG;
+                const uint32_t tp = tmem + lane_base + K::kColP;
+                if (jbA <= q) {
+                    uint32_t pk[16];
+                    p_block(pk, tg + 32 * jbA, jbA, q, lane, r, sl);
+                    tmem_st16(tp + 16 * jbA, pk);
+                }
+                if (jbB <= q) {
+                    uint32_t pk[16];
+                    p_block(pk, tg + 32 * jbB, jbB, q, lane, r, sl);
+                    tmem_st16(tp + 16 * jbB, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sm.g_empty);
+                mbar_arrive(&sm.p_full);
+                // the previous full tile's y (its Y_diag has completed: P was free)
+                if (have_pend) {
+                    if (!epilogue(j - 1)) { ok = false; break; }
+                    have_pend = false;
+                }
+            }
+
+            // S3: H = exp(cum_last) H + S^T, and (on a full tile that is not the item's last)
+            // bf16 h^T for the next tile's Y_off, once this tile's Y_off has read the old one
             const float clast2 = sl.clast2;
             const float decay = ex2(clast2);    // exp(cum_last)
             item_logd += clast2;
-            const int gb = j % K::kGBuf;
-            const uint32_t jpar = (uint32_t)j & 1u;
-
-            if (full_tile) {
-                // column blocks 2 and 3 of P
-                if (!wait_warp(&sm.g_full[gb], (uint32_t)(j / K::kGBuf) & 1u, sm, p)) break;
-                tc_fence_after();
-                const uint32_t tg = tmem + lane_base + K::kColG + gb * 128;
-#pragma unroll 1
-                for (int jb = 2; jb < 4; ++jb) p_block(tg + jb * 32, jb, q, lane, r, sl);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&sm.p_full_b);
-            }
-
-            // S3: H = exp(cum_last) H + S^T
-            if (!wait_warp(&sm.s_full, par, sm, p)) break;
+            const bool write_ht = full_tile && !last_of_item;
+            if (!wait_warp(&sm.s_full, par, sm, p)) { ok = false; break; }
+            if (write_ht && !wait_warp(&sm.h_empty, (uint32_t)j & 1u, sm, p)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll 1
-            for (int cb = 0; cb < 2 * K::kMB; ++cb) {
-                float sv[32], hv[32];
-                tmem_ld32x2(tmem + lane_base + K::kColS + cb * 32, sv, th + cb * 32, hv);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) hv[i] = fmaf(decay, hv[i], sv[i]);
-                tmem_st32(th + cb * 32, hv);
+            for (int mb = 0; mb < K::kMB; ++mb) {
+                float sv[32];
+                tmem_ld32(tmem + lane_base + K::kColS + mb * kPS + c0, sv);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) h[mb * 32 + i] = fmaf(decay, h[mb * 32 + i], sv[i]);
             }
             tc_fence_before();
             mbar_arrive(&sm.s_empty);
-            const bool last_of_item = !nx.valid || nx.item != c.item;
+            if (write_ht) {
+                ht_write<NS>(h, smem + K::kOffHt, r, hsel);
+                fence_proxy_async_smem();
+                mbar_arrive(&sm.h_full);
+            }
+            const float e_r = sl.e[r];
+            mbar_arrive(&sm.x_empty[xs]);        // the MMA adds its own arrival after Y_diag
 
+            // this tile's y is deferred to the next full tile
             if (full_tile) {
-                // h^T for the next tile's Y_off, once this tile's Y_off has read the old one
-                if (!last_of_item) {
-                    if (!wait_warp(&sm.h_empty, jpar, sm, p)) break;
-                    ht_from_state<NS>(th, r, sbase + K::kOffHt);
-                    mbar_arrive(&sm.h_full);
-                }
-                // S4: y = Y_diag + exp(cum) Y_off + D x
-                if (!wait_warp(&sm.y_full, jpar, sm, p)) break;
-                tc_fence_after();
-                const float e_r = sl.e[r];
                 const int64_t t = (int64_t)c.k * kTile + r;
-                const uint32_t xrow = sbase + K::kOffX + xs * kTileBytes;
-                __nv_bfloat16* yrow = p.y + ((uc.b * p.L + t) * p.H + uc.h) * p.P + uc.ps * kPS;
-#pragma unroll 1
-                for (int qc = 0; qc < 4; ++qc) {
-                    float yd[16], yo[16];
-                    tmem_ld16x2(tmem + lane_base + K::kColY + qc * 16, yd,
-                                tmem + lane_base + K::kColYoff + qc * 16, yo);
+                pend.row = t < p.L ? p.y + (((int64_t)uc.b * p.L + t) * p.H + uc.h) * p.P +
+                                         uc.ps * kPS + c0
+                                   : nullptr;
+                pend.e = e_r;
+                pend.d = Dh;
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const uint4 xv = ld_shared_v4(xrow + sw128_off(r, qc * 2 + cc));
-                        const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
-                        uint32_t o[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i0 = cc * 8 + e * 2;
-                            const float v0 =
-                                fmaf(Dh, bf16lo_to_f32(xin[e]), fmaf(e_r, yo[i0], yd[i0]));
-                            const float v1 =
-                                fmaf(Dh, bf16hi_to_f32(xin[e]), fmaf(e_r, yo[i0 + 1], yd[i0 + 1]));
-                            o[e] = pack_bf16x2(v0, v1);
-                        }
-                        if (t < p.L)
-                            *reinterpret_cast<uint4*>(yrow + qc * 16 + cc * 8) =
-                                make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&sm.y_empty);
+                for (int cc = 0; cc < 4; ++cc) pend.x[cc] = xk[cc];
+                have_pend = true;
                 ++j;
             }
-            mbar_arrive(&sm.x_empty[xs]);
 
             if (last_of_item && c.it.fin != kFinNone) {
                 // ---- end of an item: final state, or publish for the next range
-                float* dst = nullptr;
                 if (c.it.fin == kFinFinal) {
-                    if (p.hT) dst = p.hT + (uc.bh * p.P + (int64_t)uc.ps * kPS) * p.N;
+                    if (p.hT)
+                        h_to<NS>(h, p.hT + ((int64_t)uc.bh * p.P + (int64_t)uc.ps * kPS) * p.N, p.N,
+                                 r, c0);
                 } else {
-                    dst = p.slots + (int64_t)blockIdx.x * 2 * kPS * NS +
-                          (c.it.fin == kFinAgg ? kPS * NS : 0);
+                    publish<NS>(h, p, w, lane, r, c0, c.it.fin, item_logd);
                 }
-                state_end<NS>(p, th, q, lane, c.it.fin, dst, item_logd);
             }
-            c = nx;
         }
+        if (ok && have_pend) epilogue(j - 1);
     }
 
     // single-lane roles (TMA, MMA issue) reconverge their warp before the CTA barrier
