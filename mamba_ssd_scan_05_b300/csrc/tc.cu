@@ -70,8 +70,11 @@ struct DtSlot {
     float e[kTile];         // exp2(cum2): decay from the tile start (off-diagonal rows)
     float urow[kTile];      // exp2(cum2 - m_q), m_q = cum2[32 q - 1], q = row / 32 >= 1
     float colf[3][kTile];   // exp2(m_q - pcol), q = 1..3 (used for columns j < 32 q)
+    float rd[kTile];        // exp2(cum2 - d_q), d_q = cum2[32 q + 15]: diagonal-block row factor
+    float cd[kTile];        // exp2(d_q - pcol): diagonal-block column factor
     float clast2;           // cum2[kTile - 1]
-    float pad[3];
+    int dfac[3];            // bit q: the diagonal block of quarter q uses rd / cd (its decay
+                            // range is small enough for both factors to stay in fp32 range)
 };
 
 template <int NS>
@@ -342,6 +345,20 @@ __device__ __forceinline__ void p_block(uint32_t (&pk)[16], uint32_t tg, int jb,
             g[4 * i + 1] *= c.y * ur;
             g[4 * i + 2] *= c.z * ur;
             g[4 * i + 3] *= c.w * ur;
+        }
+    } else if ((sl.dfac[0] >> q) & 1) {
+        // diagonal block with factors around its middle row: L_ij dt_j = rd_i cd_j (j <= i)
+        const float rr = sl.rd[r];
+        const float4* cf = reinterpret_cast<const float4*>(&sl.cd[jb * 32]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 c = cf[i];
+            const float cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int jj = 4 * i + e;
+                g[jj] = (jj <= lane) ? g[jj] * cv[e] * rr : 0.f;
+            }
         }
     } else {
         const float c2 = sl.cum2[r];
@@ -640,6 +657,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m3 = __shfl_sync(0xffffffffu, incl, 23);   // token 95
             const int q = lane >> 3;
             const float mq = q == 1 ? m1 : (q == 2 ? m2 : m3);
+            // middle of this lane's 32-token block (token 32 q + 15 = lane 8 q + 3, entry 3)
+            const float dq = __shfl_sync(0xffffffffu, incl, 8 * q + 3);
+            // decay range of each 32-token block, in log2 units (cum2 is non-increasing)
+            const float blk_first = __shfl_sync(0xffffffffu, excl + cs[0], 8 * q);
+            const float blk_last = __shfl_sync(0xffffffffu, incl, 8 * q + 7);
+            float v_rd[4], v_cd[4];
             float v_c[4], v_p[4], v_w[4], v_e[4], v_u[4], v_f1[4], v_f2[4], v_f3[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -653,6 +676,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v_f1[i] = ex2(m1 - pc);
                 v_f2[i] = ex2(m2 - pc);
                 v_f3[i] = ex2(m3 - pc);
+                v_rd[i] = ex2(c2 - dq);
+                v_cd[i] = ex2(dq - pc);
             }
             DtSlot& sl = slots[s];
             const int o = 4 * lane;
@@ -667,7 +692,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float4(v_f2[0], v_f2[1], v_f2[2], v_f2[3]);
             *reinterpret_cast<float4*>(&sl.colf[2][o]) =
                 make_float4(v_f3[0], v_f3[1], v_f3[2], v_f3[3]);
-            if (lane == 0) sl.clast2 = clast2;
+            *reinterpret_cast<float4*>(&sl.rd[o]) = make_float4(v_rd[0], v_rd[1], v_rd[2], v_rd[3]);
+            *reinterpret_cast<float4*>(&sl.cd[o]) = make_float4(v_cd[0], v_cd[1], v_cd[2], v_cd[3]);
+            // |cum2_i - d_q| and |d_q - cum2_j| stay below 100 when the block's range does;
+            // dt <= 2^20 keeps cd below 2^120
+            const unsigned small = __ballot_sync(0xffffffffu, (lane & 7) == 0 &&
+                                                                  blk_first - blk_last < 100.f &&
+                                                                  blk_first - blk_last >= 0.f);
+            if (lane == 0) {
+                sl.clast2 = clast2;
+                sl.dfac[0] = (int)((small & 1u) | ((small >> 8) & 1u) << 1 |
+                                   ((small >> 16) & 1u) << 2 | ((small >> 24) & 1u) << 3);
+            }
             mbar_arrive(&sm.x_full[s]);
         }
         if (sm.abort_flag && lane == 0) {
