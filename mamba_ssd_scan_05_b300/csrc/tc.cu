@@ -25,12 +25,14 @@
 // predecessor range ends with through a decoupled look-back over per-CTA slots in the
 // workspace (inclusive states, or aggregates (decay, local state) of range pieces).
 //
-// Warp roles (352 threads):
+// Warp roles (384 threads; the producer warpgroup runs with 72 registers per thread so that
+// the compute warpgroups get 216):
 //   warp 0      TMA producer of the B / C ring (2 stages for d_state 128)
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
 //   warp 2      producer of the x / decay ring: TMA of the x tile, and from dt the tile's
 //               log2-domain cumsum and every exponential factor the other roles need
-//   warps 3-10  two identical compute warpgroups; warpgroup g (warps 3+4g .. 6+4g) owns
+//   warp 3      idle (completes the producer warpgroup)
+//   warps 4-11  two identical compute warpgroups; warpgroup g (warps 4+4g .. 7+4g) owns
 //               headdim columns 32g .. 32g+31 of x, the state and y, and half of P's column
 //               blocks.  Per tile: scaled copy of x for the state GEMM, its P blocks, the
 //               state recurrence in registers and bf16 h^T for the next off-diagonal GEMM;
@@ -53,8 +55,13 @@ using namespace ptx;
 
 constexpr int kTile = 128;          // tokens per tile (MMA M)
 constexpr int kPS = 64;             // headdim columns per unit (MMA N of Y, Y_off, S)
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDt = 2, kWarpC = 3;   // compute: warps 3..10
-constexpr int kThreads = 11 * 32;
+// warps 0-3: producers (warp 3 idle); warps 4-11: compute
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDt = 2, kWarpC = 4;
+constexpr int kThreads = 12 * 32;
+// registers per thread: launch budget, producer warpgroup, compute warpgroups
+// (4 x 32 x kRegsProducer + 8 x 32 x kRegsCompute = kThreads x kRegsLaunch)
+constexpr int kRegsLaunch = 168, kRegsProducer = 72, kRegsCompute = 216;
+static_assert(128 * kRegsProducer + 256 * kRegsCompute <= kThreads * kRegsLaunch, "registers");
 constexpr int kComputeThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTileBytes = kTile * 128;   // a 128-row x 128-byte swizzled tile (16 KB)
@@ -304,13 +311,11 @@ __device__ __forceinline__ void flag_abort(Small& sm, uint8_t* ws) {
 // Bounded wait for the completion of the phase with `parity`.  False on timeout or abort.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Small& sm,
                                          const TcParams& p) {
-    long long t0 = -1;
+    if (__builtin_expect(mbar_try_wait(bar, parity), 1)) return true;
+    const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) return false;
-        const long long t = clock64();
-        if (t0 < 0) {
-            t0 = t;
-        } else if (t - t0 > p.budget) {
+        if (__builtin_expect(*reinterpret_cast<volatile int*>(&sm.abort_flag), 0)) return false;
+        if (__builtin_expect(clock64() - t0 > p.budget, 0)) {
             flag_abort(sm, p.ws);
             return false;
         }
@@ -326,15 +331,13 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Small&
 }
 
 // One 32 x 32 block (rows 32q .. 32q+31, columns 32jb .. 32jb+31) of P = L o G o dt_j for this
-// lane's row: G's block is read from TMEM (tg) and the bf16 pairs are returned in pk.  Strictly
+// lane's row: g holds G's block (read from TMEM by the caller); the bf16 pairs go to pk.  Strictly
 // below the diagonal block every L_ij factors exactly as exp(cum_i - m) exp(m - cum_j) with
 // m = cum at row 32q - 1 (between cum_i and cum_j), so the block needs no exponential; the
 // diagonal block is masked before the exponential.  (Blocks above the diagonal are zero and
 // are written once, at kernel start.)
-__device__ __forceinline__ void p_block(uint32_t (&pk)[16], uint32_t tg, int jb, int q, int lane,
+__device__ __forceinline__ void p_block(uint32_t (&pk)[16], float (&g)[32], int jb, int q, int lane,
                                         int r, const DtSlot& sl) {
-    float g[32];
-    tmem_ld32(tg, g);
     if (jb < q) {
         const float ur = sl.urow[r];
         const float4* cf = reinterpret_cast<const float4*>(&sl.colf[q - 1][jb * 32]);
@@ -346,7 +349,7 @@ __device__ __forceinline__ void p_block(uint32_t (&pk)[16], uint32_t tg, int jb,
             g[4 * i + 2] *= c.z * ur;
             g[4 * i + 3] *= c.w * ur;
         }
-    } else if ((sl.dfac[0] >> q) & 1) {
+    } else if (__builtin_expect((sl.dfac[0] >> q) & 1, 1)) {
         // diagonal block with factors around its middle row: L_ij dt_j = rd_i cd_j (j <= i)
         const float rr = sl.rd[r];
         const float4* cf = reinterpret_cast<const float4*>(&sl.cd[jb * 32]);
@@ -577,6 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
 
+    if (warp < kWarpC) {
+    regs_dec<kRegsProducer>();
     if (warp == kWarpTma) {
         // ------------------------------------------------------- B / C TMA producer ----
         if (lane == 0) {
@@ -836,7 +841,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (!mbar_try_wait(&sm.mma_done, 0) && clock64() - t0 < p.budget) {
             }
         }
+    }
     } else {
+        regs_inc<kRegsCompute>();
         // ------------------------------------------------------------- compute warps -----
         const int w = warp - kWarpC;             // 0..7
         const int q = warp & 3;                  // TMEM lane quarter
@@ -855,11 +862,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int yb = pj % K::kYBuf;
             if (!wait_warp(&sm.y_full[yb], (uint32_t)(pj / K::kYBuf) & 1u, sm, p)) return false;
             tc_fence_after();
+            float yd[32], yo[32];
+            tmem_ld32x2(tmem + lane_base + K::kColY + yb * kPS + c0, yd,
+                        tmem + lane_base + K::kColYoff + yb * kPS + c0, yo);
 #pragma unroll
             for (int qc = 0; qc < 2; ++qc) {
-                float yd[16], yo[16];
-                tmem_ld16x2(tmem + lane_base + K::kColY + yb * kPS + c0 + qc * 16, yd,
-                            tmem + lane_base + K::kColYoff + yb * kPS + c0 + qc * 16, yo);
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const uint4 xv = pend.x[qc * 2 + cc];
@@ -867,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t o[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int i0 = cc * 8 + e * 2;
+                        const int i0 = qc * 16 + cc * 8 + e * 2;
                         const float v0 =
                             fmaf(pend.d, bf16lo_to_f32(xin[e]), fmaf(pend.e, yo[i0], yd[i0]));
                         const float v1 = fmaf(pend.d, bf16hi_to_f32(xin[e]),
@@ -895,11 +902,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t par = (uint32_t)nt & 1u;
             const bool last_of_item = c.k + 1 == c.it.k1;
             if (c.k == c.it.k0) {
-                // ---- start of an item: flush the deferred epilogue, then the entering state
-                if (have_pend) {
-                    if (!epilogue(j - 1)) { ok = false; break; }
-                    have_pend = false;
-                }
+                // ---- start of an item: the entering state (a deferred epilogue of the previous
+                // item runs after this item's first P, like any other)
                 item_logd = 0.f;
                 if (c.it.u != d_u) {
                     d_u = c.it.u;
@@ -959,15 +963,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t tg = tmem + lane_base + K::kColG;
                 const uint32_t tp = tmem + lane_base + K::kColP;
-                if (jbA <= q) {
+#pragma unroll 1
+                for (int bi = 0; bi < 2; ++bi) {
+                    const int jb = bi ? jbB : jbA;
+                    if (jb > q) continue;
+                    float g[32];
+                    tmem_ld32(tg + 32 * jb, g);
                     uint32_t pk[16];
-                    p_block(pk, tg + 32 * jbA, jbA, q, lane, r, sl);
-                    tmem_st16(tp + 16 * jbA, pk);
-                }
-                if (jbB <= q) {
-                    uint32_t pk[16];
-                    p_block(pk, tg + 32 * jbB, jbB, q, lane, r, sl);
-                    tmem_st16(tp + 16 * jbB, pk);
+                    p_block(pk, g, jb, q, lane, r, sl);
+                    tmem_st16(tp + 16 * jb, pk);
                 }
                 tmem_wait_st();
                 tc_fence_before();

@@ -268,6 +268,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         : "memory");
 }
 
+// ---- register reallocation between warpgroups -------------------------------------------
+
+// Lower / raise this warpgroup's per-thread register count (all four warps of the warpgroup
+// execute it).  The raises of a CTA must fit in what the CTA was launched with.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---- global flags (cross-CTA hand-off) ------------------------------------------------------
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* a) {
