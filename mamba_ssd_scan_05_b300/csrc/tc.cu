@@ -384,33 +384,37 @@ __device__ __forceinline__ void p_block(uint32_t (&pk)[16], float (&g)[32], int 
 // ---- the state in registers of the compute threads -------------------------------------------
 // Compute thread (row r, column half c0) holds h^T rows n = 128 mb + r, columns p = c0 .. c0+31.
 
-// h <- scale * src + h when `accumulate`, else h <- src.  src is a [64 x N] fp32 block (element
-// (p, n) at p * ld + n); nullptr means zeros.  `l2only` reads bypass L1 (for states another SM
-// published).
+// h <- scale * src + h when `accumulate`, else h <- src.  src is a [64 x NS] fp32 block
+// (element (p, n) at p * NS + n: the state layout, whose row length is d_state); nullptr means
+// zeros.  `l2only` reads bypass L1 (for states another SM published).  The element offsets
+// are compile-time constants from one base address.
 template <int NS>
-__device__ __forceinline__ void h_from(float (&h)[NS / 4], const float* src, int64_t ld, int r,
-                                       int c0, float scale, bool accumulate, bool l2only) {
+__device__ __forceinline__ void h_from(float (&h)[NS / 4], const float* src, int r, int c0,
+                                       float scale, bool accumulate, bool l2only) {
+    if (!src) {
+#pragma unroll
+        for (int i = 0; i < NS / 4; ++i) h[i] = accumulate ? h[i] : 0.f;
+        return;
+    }
+    const float* base = src + (int64_t)c0 * NS + r;
 #pragma unroll
     for (int mb = 0; mb < NS / 128; ++mb)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            float x = 0.f;
-            if (src) {
-                const float* a = src + (int64_t)(c0 + i) * ld + mb * 128 + r;
-                x = l2only ? __ldcg(a) : *a;
-            }
+            const float* a = base + i * NS + mb * 128;
+            const float x = l2only ? __ldcg(a) : *a;
             h[mb * 32 + i] = accumulate ? fmaf(scale, x, h[mb * 32 + i]) : x;
         }
 }
 
-// dst[p][n] <- h (fp32)
+// dst[p][n] <- h (fp32), dst a [64 x NS] block with rows of d_state elements
 template <int NS>
-__device__ __forceinline__ void h_to(const float (&h)[NS / 4], float* dst, int64_t ld, int r,
-                                     int c0) {
+__device__ __forceinline__ void h_to(const float (&h)[NS / 4], float* dst, int r, int c0) {
+    float* base = dst + (int64_t)c0 * NS + r;
 #pragma unroll
     for (int mb = 0; mb < NS / 128; ++mb)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dst[(int64_t)(c0 + i) * ld + mb * 128 + r] = h[mb * 32 + i];
+        for (int i = 0; i < 32; ++i) base[i * NS + mb * 128] = h[mb * 32 + i];
 }
 
 // bf16 h^T into the MN-major, 128-byte swizzled tile (N rows x 64 columns) at ht: the B operand
@@ -441,7 +445,7 @@ template <int NS>
 __device__ __forceinline__ bool look_back(float (&h)[NS / 4], const TcParams& p, Small& sm,
                                           int w, int lane, int r, int c0) {
     const int64_t slot_elems = (int64_t)kPS * NS;
-    h_from<NS>(h, nullptr, NS, r, c0, 0.f, false, false);
+    h_from<NS>(h, nullptr, r, c0, 0.f, false, false);
     float acc_logd = 0.f;
 #pragma unroll 1
     for (int jp = (int)blockIdx.x - 1; jp >= 0; --jp) {
@@ -464,7 +468,7 @@ __device__ __forceinline__ bool look_back(float (&h)[NS / 4], const TcParams& p,
         // every lane acquires the flag itself before it reads the published state
         (void)ld_acquire_gpu(f + kind - 1);
         const float* slot = p.slots + (int64_t)jp * 2 * slot_elems + (kind == 2 ? slot_elems : 0);
-        h_from<NS>(h, slot, NS, r, c0, ex2(acc_logd), true, true);
+        h_from<NS>(h, slot, r, c0, ex2(acc_logd), true, true);
         if (kind == 1) return true;
         acc_logd += __int_as_float(__ldcg(f + 2));
     }
@@ -478,7 +482,7 @@ __device__ __forceinline__ void publish(const float (&h)[NS / 4], const TcParams
                                         int lane, int r, int c0, int fin, float item_logd) {
     const int64_t slot_elems = (int64_t)kPS * NS;
     float* slot = p.slots + (int64_t)blockIdx.x * 2 * slot_elems + (fin == kFinAgg ? slot_elems : 0);
-    h_to<NS>(h, slot, NS, r, c0);
+    h_to<NS>(h, slot, r, c0);
     __threadfence();
     __syncwarp();
     if (lane == 0) {
@@ -913,9 +917,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!look_back<NS>(h, p, sm, w, lane, r, c0)) { ok = false; break; }
                 } else {
                     const float* src = (c.it.init == kInitH0 && p.h0)
-                                           ? p.h0 + ((int64_t)uc.bh * p.P + (int64_t)uc.ps * kPS) * p.N
+                                           ? p.h0 + ((int64_t)uc.bh * p.P + (int64_t)uc.ps * kPS) * NS
                                            : nullptr;
-                    h_from<NS>(h, src, p.N, r, c0, 0.f, false, false);
+                    h_from<NS>(h, src, r, c0, 0.f, false, false);
                 }
                 if (full_tile) {
                     // h^T for the item's first Y_off, once the previous full tile's Y_off is done
@@ -1028,8 +1032,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- end of an item: final state, or publish for the next range
                 if (c.it.fin == kFinFinal) {
                     if (p.hT)
-                        h_to<NS>(h, p.hT + ((int64_t)uc.bh * p.P + (int64_t)uc.ps * kPS) * p.N, p.N,
-                                 r, c0);
+                        h_to<NS>(h, p.hT + ((int64_t)uc.bh * p.P + (int64_t)uc.ps * kPS) * NS, r,
+                                 c0);
                 } else {
                     publish<NS>(h, p, w, lane, r, c0, c.it.fin, item_logd);
                 }
