@@ -55,14 +55,8 @@ using namespace ptx;
 
 constexpr int kTile = 128;          // tokens per tile (MMA M)
 constexpr int kPS = 64;             // headdim columns per unit (MMA N of Y, Y_off, S)
-// warps 0-3: producers (warp 3 idle); warps 4-11: compute
+// warps 0-3: producers (warp 3 idle); warps 4 ...: compute warpgroups
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDt = 2, kWarpC = 4;
-constexpr int kThreads = 12 * 32;
-// registers per thread: launch budget, producer warpgroup, compute warpgroups
-// (4 x 32 x kRegsProducer + 8 x 32 x kRegsCompute = kThreads x kRegsLaunch)
-constexpr int kRegsLaunch = 168, kRegsProducer = 72, kRegsCompute = 216;
-static_assert(128 * kRegsProducer + 256 * kRegsCompute <= kThreads * kRegsLaunch, "registers");
-constexpr int kComputeThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTileBytes = kTile * 128;   // a 128-row x 128-byte swizzled tile (16 KB)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -91,7 +85,21 @@ struct Cfg {
     static constexpr int kBCStages = NS == 128 ? 2 : 1;
     static constexpr int kYBuf = NS == 128 ? 2 : 1;   // Y / Y_off accumulator buffers
     static constexpr int kMB = NS / 128;               // 128-row blocks of the state
-    static constexpr int kHReg = kMB * 32;             // state values per compute thread
+    // compute warpgroups; each owns kCW of the unit's 64 headdim columns (and kPB of P's
+    // 32-column blocks per lane quarter)
+    static constexpr int kWG = NS == 128 ? 4 : 2;
+    static constexpr int kCW = kPS / kWG;
+    static constexpr int kPB = 4 / kWG;
+    static constexpr int kHReg = kMB * kCW;            // state values per compute thread
+    static constexpr int kComputeThreads = 128 * kWG;
+    static constexpr int kThreads = 128 + kComputeThreads;
+    // registers per thread: launch budget, producer warpgroup, compute warpgroups
+    static constexpr int kRegsLaunch = NS == 128 ? 96 : 168;
+    static constexpr int kRegsProducer = NS == 128 ? 64 : 88;
+    static constexpr int kRegsCompute = NS == 128 ? 104 : 208;
+    static_assert(128 * kRegsProducer + kComputeThreads * kRegsCompute <= kThreads * kRegsLaunch,
+                  "registers");
+    static_assert(kThreads * kRegsLaunch <= 65536, "register file");
     static constexpr uint32_t kBCBytes = 2 * kNReg * kTileBytes;
     // shared memory (byte offsets from a 1024-aligned base)
     static constexpr uint32_t kOffX = 0;
@@ -303,6 +311,21 @@ __device__ __forceinline__ void advance(Cursor& c, const Plan& pl, const Small& 
     }
 }
 
+// advance for the producer roles: the item change is one out-of-line copy.
+__device__ __noinline__ Cursor next_item(Cursor c, const Plan* pl, const Small* sm,
+                                         const TcParams* p) {
+    advance(c, *pl, *sm, *p);
+    return c;
+}
+__device__ __forceinline__ void advance_p(Cursor& c, const Plan& pl, const Small& sm,
+                                          const TcParams& p) {
+    if (__builtin_expect(c.valid && c.k + 1 < c.it.k1, 1)) {
+        ++c.k;
+        return;
+    }
+    c = next_item(c, &pl, &sm, &p);
+}
+
 __device__ __forceinline__ void flag_abort(Small& sm, uint8_t* ws) {
     *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
     set_status(ws, SSD_ERR_TIMEOUT);
@@ -323,11 +346,31 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Small& 
     return true;
 }
 
+// wait_bar for the single-lane producer roles: the slow path is one out-of-line copy (a call
+// is cheap there, with few live registers), which keeps their hot code small.
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, Small* sm,
+                                           const TcParams* p) {
+    return wait_bar(bar, parity, *sm, *p);
+}
+__device__ __forceinline__ bool wait_bar_p(uint64_t* bar, uint32_t parity, Small& sm,
+                                           const TcParams& p) {
+    if (__builtin_expect(mbar_try_wait(bar, parity), 1)) return true;
+    return wait_bar_slow(bar, parity, &sm, &p);
+}
+
 // wait_bar for the 32 lanes of a warp, with one verdict for the whole warp, so the warp stays
 // converged for the .sync.aligned TMEM instructions that follow.
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Small& sm,
                                           const TcParams& p) {
     return __all_sync(0xffffffffu, wait_bar(bar, parity, sm, p));
+}
+
+// wait_warp for a producer role run by a whole warp, with the slow path out of line.
+__device__ __forceinline__ bool wait_warp_p(uint64_t* bar, uint32_t parity, Small& sm,
+                                            const TcParams& p) {
+    const bool ok = mbar_try_wait(bar, parity);
+    if (__builtin_expect(__all_sync(0xffffffffu, ok), 1)) return true;
+    return __all_sync(0xffffffffu, ok || wait_bar_slow(bar, parity, &sm, &p));
 }
 
 // One 32 x 32 block (rows 32q .. 32q+31, columns 32jb .. 32jb+31) of P = L o G o dt_j for this
@@ -382,70 +425,73 @@ __device__ __forceinline__ void p_block(uint32_t (&pk)[16], float (&g)[32], int 
 }
 
 // ---- the state in registers of the compute threads -------------------------------------------
-// Compute thread (row r, column half c0) holds h^T rows n = 128 mb + r, columns p = c0 .. c0+31.
+// Compute thread (row r, column block c0) holds h^T rows n = 128 mb + r, columns
+// p = c0 .. c0 + CW - 1 (CW headdim columns per compute warpgroup).
 
 // h <- scale * src + h when `accumulate`, else h <- src.  src is a [64 x NS] fp32 block
 // (element (p, n) at p * NS + n: the state layout, whose row length is d_state); nullptr means
 // zeros.  `l2only` reads bypass L1 (for states another SM published).  The element offsets
 // are compile-time constants from one base address.
-template <int NS>
-__device__ __forceinline__ void h_from(float (&h)[NS / 4], const float* src, int r, int c0,
+template <int NS, int CW>
+__device__ __forceinline__ void h_from(float (&h)[NS / 128 * CW], const float* src, int r, int c0,
                                        float scale, bool accumulate, bool l2only) {
     if (!src) {
 #pragma unroll
-        for (int i = 0; i < NS / 4; ++i) h[i] = accumulate ? h[i] : 0.f;
+        for (int i = 0; i < NS / 128 * CW; ++i) h[i] = accumulate ? h[i] : 0.f;
         return;
     }
     const float* base = src + (int64_t)c0 * NS + r;
 #pragma unroll
     for (int mb = 0; mb < NS / 128; ++mb)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < CW; ++i) {
             const float* a = base + i * NS + mb * 128;
             const float x = l2only ? __ldcg(a) : *a;
-            h[mb * 32 + i] = accumulate ? fmaf(scale, x, h[mb * 32 + i]) : x;
+            h[mb * CW + i] = accumulate ? fmaf(scale, x, h[mb * CW + i]) : x;
         }
 }
 
 // dst[p][n] <- h (fp32), dst a [64 x NS] block with rows of d_state elements
-template <int NS>
-__device__ __forceinline__ void h_to(const float (&h)[NS / 4], float* dst, int r, int c0) {
+template <int NS, int CW>
+__device__ __forceinline__ void h_to(const float (&h)[NS / 128 * CW], float* dst, int r, int c0) {
     float* base = dst + (int64_t)c0 * NS + r;
 #pragma unroll
     for (int mb = 0; mb < NS / 128; ++mb)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) base[i * NS + mb * 128] = h[mb * 32 + i];
+        for (int i = 0; i < CW; ++i) base[i * NS + mb * 128] = h[mb * CW + i];
 }
 
 // bf16 h^T into the MN-major, 128-byte swizzled tile (N rows x 64 columns) at ht: the B operand
 // of the next off-diagonal GEMM.
-template <int NS>
-__device__ __forceinline__ void ht_write(const float (&h)[NS / 4], uint8_t* ht, int r, int hsel) {
+// wg is the thread's column block (its 16-byte chunks are wg * CW / 8 ...).
+template <int NS, int CW>
+__device__ __forceinline__ void ht_write(const float (&h)[NS / 128 * CW], uint8_t* ht, int r,
+                                         int wg) {
 #pragma unroll
     for (int mb = 0; mb < NS / 128; ++mb)
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const float* v = &h[mb * 32 + cc * 8];
-            *reinterpret_cast<uint4*>(ht + sw128_off(mb * 128 + r, hsel * 4 + cc)) =
+        for (int cc = 0; cc < CW / 8; ++cc) {
+            const float* v = &h[mb * CW + cc * 8];
+            *reinterpret_cast<uint4*>(ht + sw128_off(mb * 128 + r, wg * (CW / 8) + cc)) =
                 make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
         }
 }
 
 // Flags of the state hand-off between CTAs, per CTA and per compute warp w (the warp that owns
-// state rows 32q .. 32q+31 of every 128-row block and one column half): [0] inclusive state
+// state rows 32q .. 32q+31 of every 128-row block and one column block): [0] inclusive state
 // published, [1] aggregate published, [2] the aggregate's log2 decay.  A warp only needs the
 // same part of its predecessor's state, so publishing and looking back are per warp.
-constexpr int kFlagsPerCta = 32;
+constexpr int kFlagsPerCta = 64;   // 4 words for each of up to 16 compute warps
 
 // Decoupled look-back over the preceding ranges' published states (per compute warp):
 //     h_in = D_1 (D_2 (... h_incl ...) + H_2) + H_1.
 // False on timeout or abort.
-template <int NS>
-__device__ __forceinline__ bool look_back(float (&h)[NS / 4], const TcParams& p, Small& sm,
+template <int NS, int CW>
+__device__ __forceinline__ bool look_back(float (&h)[NS / 128 * CW], const TcParams& p, Small& sm,
                                           int w, int lane, int r, int c0) {
     const int64_t slot_elems = (int64_t)kPS * NS;
-    h_from<NS>(h, nullptr, r, c0, 0.f, false, false);
+    h_from<NS, CW>(h, nullptr, r, c0, 0.f, false, false);
     float acc_logd = 0.f;
 #pragma unroll 1
     for (int jp = (int)blockIdx.x - 1; jp >= 0; --jp) {
@@ -468,7 +514,7 @@ __device__ __forceinline__ bool look_back(float (&h)[NS / 4], const TcParams& p,
         // every lane acquires the flag itself before it reads the published state
         (void)ld_acquire_gpu(f + kind - 1);
         const float* slot = p.slots + (int64_t)jp * 2 * slot_elems + (kind == 2 ? slot_elems : 0);
-        h_from<NS>(h, slot, r, c0, ex2(acc_logd), true, true);
+        h_from<NS, CW>(h, slot, r, c0, ex2(acc_logd), true, true);
         if (kind == 1) return true;
         acc_logd += __int_as_float(__ldcg(f + 2));
     }
@@ -477,12 +523,12 @@ __device__ __forceinline__ bool look_back(float (&h)[NS / 4], const TcParams& p,
 
 // This warp's part of the CTA's inclusive state (kFinIncl) or aggregate (kFinAgg), published
 // for the next range.
-template <int NS>
-__device__ __forceinline__ void publish(const float (&h)[NS / 4], const TcParams& p, int w,
+template <int NS, int CW>
+__device__ __forceinline__ void publish(const float (&h)[NS / 128 * CW], const TcParams& p, int w,
                                         int lane, int r, int c0, int fin, float item_logd) {
     const int64_t slot_elems = (int64_t)kPS * NS;
     float* slot = p.slots + (int64_t)blockIdx.x * 2 * slot_elems + (fin == kFinAgg ? slot_elems : 0);
-    h_to<NS>(h, slot, r, c0);
+    h_to<NS, CW>(h, slot, r, c0);
     __threadfence();
     __syncwarp();
     if (lane == 0) {
@@ -494,15 +540,37 @@ __device__ __forceinline__ void publish(const float (&h)[NS / 4], const TcParams
 }
 
 // A tile whose y epilogue is deferred by one tile (always the previous full tile).
+template <int CW>
 struct PendingY {
-    __nv_bfloat16* row;     // y row at this thread's column half, or null past the sequence end
+    __nv_bfloat16* row;     // y row at this thread's column block, or null past the sequence end
     float e;                // exp(cum) of the row
     float d;                // D of the head
-    uint4 x[4];             // x row, this thread's column half (bf16 pairs)
+    uint4 x[CW / 8];        // x row, this thread's column block (bf16 pairs)
 };
 
+// CW consecutive fp32 TMEM columns at ta and at tb, one wait for both
+template <int CW>
+__device__ __forceinline__ void tmem_ld_pair(uint32_t ta, float (&va)[CW], uint32_t tb,
+                                             float (&vb)[CW]) {
+    if constexpr (CW == 32) tmem_ld32x2(ta, va, tb, vb);
+    else tmem_ld16x2(ta, va, tb, vb);
+}
+template <int CW>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t ta, float (&v)[CW]) {
+    if constexpr (CW == 32) tmem_ld32(ta, v);
+    else tmem_ld16(ta, v);
+}
+
+// P column block (0..3) number bi of compute warpgroup wg: with two warpgroups each takes two
+// blocks, paired so that every lane quarter's lower-triangle blocks split evenly.
+template <int WG>
+__device__ __forceinline__ int p_col_block(int wg, int bi) {
+    if constexpr (WG == 4) return wg;
+    else return bi ? (wg ? 2 : 3) : (wg ? 1 : 0);
+}
+
 template <int NS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NS>::kThreads, 1)
     ssd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmC,
                   const __grid_constant__ TcParams p) {
@@ -519,23 +587,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < K::kXSt; ++i) {
             mbar_init(&sm.x_full[i], 1 + 32);
-            mbar_init(&sm.x_empty[i], 1 + kComputeThreads);
+            mbar_init(&sm.x_empty[i], 1 + K::kComputeThreads);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.bc_full[i], 1);
             mbar_init(&sm.bc_empty[i], 1);
             mbar_init(&sm.y_full[i], 1);
-            mbar_init(&sm.y_empty[i], kComputeThreads);
+            mbar_init(&sm.y_empty[i], K::kComputeThreads);
         }
         mbar_init(&sm.g_full, 1);
-        mbar_init(&sm.g_empty, kComputeThreads);
-        mbar_init(&sm.p_full, kComputeThreads);
+        mbar_init(&sm.g_empty, K::kComputeThreads);
+        mbar_init(&sm.p_full, K::kComputeThreads);
         mbar_init(&sm.p_empty, 1);
-        mbar_init(&sm.xt_full, kComputeThreads);
+        mbar_init(&sm.xt_full, K::kComputeThreads);
         mbar_init(&sm.xt_empty, 1);
         mbar_init(&sm.s_full, 1);
-        mbar_init(&sm.s_empty, kComputeThreads);
-        mbar_init(&sm.h_full, kComputeThreads);
+        mbar_init(&sm.s_empty, K::kComputeThreads);
+        mbar_init(&sm.h_full, K::kComputeThreads);
         mbar_init(&sm.h_empty, 1);
         mbar_init(&sm.mma_done, 1);
         sm.abort_flag = 0;
@@ -570,14 +638,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // P's blocks above the diagonal are zero in every tile: written once
     if (warp >= kWarpC) {
-        const int q = warp & 3, hsel = (warp - kWarpC) >> 2;
+        const int q = warp & 3, wg = (warp - kWarpC) >> 2;
         const uint32_t tp = tmem + ((uint32_t)(q * 32) << 16) + K::kColP;
         uint32_t z[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[i] = 0u;
-        const int jbA = hsel ? 1 : 0, jbB = hsel ? 2 : 3;
-        if (jbA > q) tmem_st16(tp + 16 * jbA, z);
-        if (jbB > q) tmem_st16(tp + 16 * jbB, z);
+#pragma unroll
+        for (int bi = 0; bi < K::kPB; ++bi) {
+            const int jb = p_col_block<K::kWG>(wg, bi);
+            if (jb > q) tmem_st16(tp + 16 * jb, z);
+        }
         tmem_wait_st();
     }
     tc_fence_before();
@@ -585,15 +655,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
 
     if (warp < kWarpC) {
-    regs_dec<kRegsProducer>();
+    regs_dec<K::kRegsProducer>();
     if (warp == kWarpTma) {
         // ------------------------------------------------------- B / C TMA producer ----
         if (lane == 0) {
             int nt = 0;
-            for (Cursor c = first_tile(plan, sm, p); c.valid; advance(c, plan, sm, p), ++nt) {
+            for (Cursor c = first_tile(plan, sm, p); c.valid; advance_p(c, plan, sm, p), ++nt) {
                 const int s = nt % K::kBCStages;
                 const uint32_t use = nt / K::kBCStages;
-                if (!wait_bar(&sm.bc_empty[s], (use & 1u) ^ 1u, sm, p)) break;
+                if (!wait_bar_p(&sm.bc_empty[s], (use & 1u) ^ 1u, sm, p)) break;
                 const int t0 = c.k * kTile;
                 // a state-only tile needs B; a full tile also C
                 mbar_arrive_expect_tx(&sm.bc_full[s],
@@ -625,16 +695,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         int nt = 0;
         int a_u = -1;
         float A2 = 0.f;
-        for (Cursor c = first_tile(plan, sm, p); c.valid; advance(c, plan, sm, p), ++nt) {
-            // dt of this tile (4 consecutive tokens per lane): in flight during the wait below
-            float d0[4];
-            {
-                const int64_t t = (int64_t)c.k * kTile + 4 * lane;
-                const __nv_bfloat16* src = p.dt + ((int64_t)c.uc.b * p.L + t) * p.H + c.uc.h;
+        // dt of tile k of the cursor's unit, 4 consecutive tokens per lane
+        auto load_dt = [&](const Cursor& c, int k, float (&d)[4]) {
+            const int64_t t = (int64_t)k * kTile + 4 * lane;
+            const __nv_bfloat16* src = p.dt + ((int64_t)c.uc.b * p.L + t) * p.H + c.uc.h;
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    d0[i] = t + i < p.L ? __bfloat162float(src[(int64_t)i * p.H]) : 0.f;
+            for (int i = 0; i < 4; ++i)
+                d[i] = t + i < p.L ? __bfloat162float(src[(int64_t)i * p.H]) : 0.f;
+        };
+        // the next tile's dt is loaded one tile ahead (when it belongs to the same unit), so
+        // its memory latency overlaps this tile's work
+        float dn[4] = {0.f, 0.f, 0.f, 0.f};
+        bool have_next = false;
+        for (Cursor c = first_tile(plan, sm, p); c.valid; advance_p(c, plan, sm, p), ++nt) {
+            float d0[4];
+            if (have_next) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) d0[i] = dn[i];
+            } else {
+                load_dt(c, c.k, d0);
             }
+            have_next = c.k + 1 < c.it.k1;
+            if (have_next) load_dt(c, c.k + 1, dn);
             if (c.it.u != a_u) {
                 a_u = c.it.u;
                 A2 = p.A[c.uc.h] * kLog2e;
@@ -671,38 +753,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             // decay range of each 32-token block, in log2 units (cum2 is non-increasing)
             const float blk_first = __shfl_sync(0xffffffffu, excl + cs[0], 8 * q);
             const float blk_last = __shfl_sync(0xffffffffu, incl, 8 * q + 7);
-            float v_rd[4], v_cd[4];
-            float v_c[4], v_p[4], v_w[4], v_e[4], v_u[4], v_f1[4], v_f2[4], v_f3[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float c2 = excl + cs[i];
-                const float pc = d0[i] > 0.f ? c2 - lg2(d0[i]) : __int_as_float(0x7f800000);
-                v_c[i] = c2;
-                v_p[i] = pc;
-                v_w[i] = ex2(clast2 - c2) * d0[i];
-                v_e[i] = ex2(c2);
-                v_u[i] = q > 0 ? ex2(c2 - mq) : 1.f;
-                v_f1[i] = ex2(m1 - pc);
-                v_f2[i] = ex2(m2 - pc);
-                v_f3[i] = ex2(m3 - pc);
-                v_rd[i] = ex2(c2 - dq);
-                v_cd[i] = ex2(dq - pc);
-            }
             DtSlot& sl = slots[s];
             const int o = 4 * lane;
-            *reinterpret_cast<float4*>(&sl.cum2[o]) = make_float4(v_c[0], v_c[1], v_c[2], v_c[3]);
-            *reinterpret_cast<float4*>(&sl.pcol[o]) = make_float4(v_p[0], v_p[1], v_p[2], v_p[3]);
-            *reinterpret_cast<float4*>(&sl.w[o]) = make_float4(v_w[0], v_w[1], v_w[2], v_w[3]);
-            *reinterpret_cast<float4*>(&sl.e[o]) = make_float4(v_e[0], v_e[1], v_e[2], v_e[3]);
-            *reinterpret_cast<float4*>(&sl.urow[o]) = make_float4(v_u[0], v_u[1], v_u[2], v_u[3]);
-            *reinterpret_cast<float4*>(&sl.colf[0][o]) =
-                make_float4(v_f1[0], v_f1[1], v_f1[2], v_f1[3]);
-            *reinterpret_cast<float4*>(&sl.colf[1][o]) =
-                make_float4(v_f2[0], v_f2[1], v_f2[2], v_f2[3]);
-            *reinterpret_cast<float4*>(&sl.colf[2][o]) =
-                make_float4(v_f3[0], v_f3[1], v_f3[2], v_f3[3]);
-            *reinterpret_cast<float4*>(&sl.rd[o]) = make_float4(v_rd[0], v_rd[1], v_rd[2], v_rd[3]);
-            *reinterpret_cast<float4*>(&sl.cd[o]) = make_float4(v_cd[0], v_cd[1], v_cd[2], v_cd[3]);
+            float c2[4], pc[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                c2[i] = excl + cs[i];
+                pc[i] = d0[i] > 0.f ? c2[i] - lg2(d0[i]) : __int_as_float(0x7f800000);
+            }
+            // each factor is stored as soon as its four values exist (few live registers)
+            auto put = [&](float* dst, auto f) {
+                *reinterpret_cast<float4*>(dst + o) = make_float4(f(0), f(1), f(2), f(3));
+            };
+            put(sl.cum2, [&](int i) { return c2[i]; });
+            put(sl.pcol, [&](int i) { return pc[i]; });
+            put(sl.w, [&](int i) { return ex2(clast2 - c2[i]) * d0[i]; });
+            put(sl.e, [&](int i) { return ex2(c2[i]); });
+            put(sl.urow, [&](int i) { return q > 0 ? ex2(c2[i] - mq) : 1.f; });
+            put(sl.colf[0], [&](int i) { return ex2(m1 - pc[i]); });
+            put(sl.colf[1], [&](int i) { return ex2(m2 - pc[i]); });
+            put(sl.colf[2], [&](int i) { return ex2(m3 - pc[i]); });
+            put(sl.rd, [&](int i) { return ex2(c2[i] - dq); });
+            put(sl.cd, [&](int i) { return ex2(dq - pc[i]); });
             // |cum2_i - d_q| and |d_q - cum2_j| stay below 100 when the block's range does;
             // dt <= 2^20 keeps cd below 2^120
             const unsigned small = __ballot_sync(0xffffffffu, (lane & 7) == 0 &&
@@ -728,28 +800,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kWarpMma) {
         // ---------------------------------------------------------------- MMA issuer ------
-        if (lane == 0) {
+        // the whole warp runs this role in converged control flow; one elected lane issues
+        {
             constexpr uint32_t idG = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idS = idesc_bf16(128, kPS, 1, 1);
             constexpr uint32_t idYoff = idesc_bf16(128, kPS, 0, 1);
             constexpr uint32_t idYd = idesc_bf16(128, kPS, 0, 1);
+            // Each K = 128 GEMM goes out as one block of 8 back-to-back MMAs from converged
+            // code (issued one by one from a loop, the tensor core takes them at about half
+            // its rate).
             // G = C B^T of tile number nt (the j-th full tile), once the P builders have read
             // the previous G
             auto issue_G = [&](int nt, int j) -> bool {
                 const int s = nt % K::kBCStages;
-                if (!wait_bar(&sm.bc_full[s], (uint32_t)(nt / K::kBCStages) & 1u, sm, p))
+                if (!wait_warp_p(&sm.bc_full[s], (uint32_t)(nt / K::kBCStages) & 1u, sm, p))
                     return false;
-                if (!wait_bar(&sm.g_empty, ((uint32_t)j & 1u) ^ 1u, sm, p)) return false;
+                if (!wait_warp_p(&sm.g_empty, ((uint32_t)j & 1u) ^ 1u, sm, p)) return false;
                 tc_fence_after();
                 const uint32_t bbase = sbase + K::kOffBC + s * K::kBCBytes;
                 const uint32_t cbase = bbase + K::kNReg * kTileBytes;
-#pragma unroll 1
-                for (int kk = 0; kk < NS / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-                    mma_f16(tmem + K::kColG, smem_desc_sw128(cbase + off, 16, 1024),
-                            smem_desc_sw128(bbase + off, 16, 1024), idG, kk > 0);
-                }
-                mma_commit(&sm.g_full);
+#pragma unroll
+                for (int kb = 0; kb < NS / 128; ++kb)
+                    mma8_ss_e<kStepCols, kStepCols>(
+                        tmem + K::kColG, smem_desc_sw128(cbase + 2 * kb * kTileBytes, 16, 1024),
+                        smem_desc_sw128(bbase + 2 * kb * kTileBytes, 16, 1024), idG, kb > 0);
+                mma_commit_e(&sm.g_full);
                 return true;
             };
             int nt = 0, j = 0;           // tiles issued, full (non state-only) tiles issued
@@ -768,109 +843,104 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (full_tile && !g_ahead && !issue_G(nt, j)) break;
                 g_ahead = false;
                 // chunk state S^T = B^T (w o X)
-                if (!wait_bar(&sm.xt_full, par, sm, p) || !wait_bar(&sm.s_empty, par ^ 1u, sm, p))
+                if (!wait_warp_p(&sm.xt_full, par, sm, p) || !wait_warp_p(&sm.s_empty, par ^ 1u, sm, p))
                     break;
                 if (!full_tile &&
-                    !wait_bar(&sm.bc_full[s], (uint32_t)(nt / K::kBCStages) & 1u, sm, p))
+                    !wait_warp_p(&sm.bc_full[s], (uint32_t)(nt / K::kBCStages) & 1u, sm, p))
                     break;
                 tc_fence_after();
                 {
                     const uint32_t bbase = sbase + K::kOffBC + s * K::kBCBytes;
                     const uint32_t xt = sbase + K::kOffXt;
-#pragma unroll 1
+#pragma unroll
                     for (int mb = 0; mb < K::kMB; ++mb)
-#pragma unroll 1
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_f16(tmem + K::kColS + mb * kPS,
-                                    smem_desc_sw128(bbase + 2 * mb * kTileBytes + kk * 2048,
-                                                    kTileBytes, 1024),
-                                    smem_desc_sw128(xt + kk * 2048, 1024, 1024), idS, kk > 0);
+                        mma8_ss_e<kStepRows, kStepRows>(
+                            tmem + K::kColS + mb * kPS,
+                            smem_desc_sw128(bbase + 2 * mb * kTileBytes, kTileBytes, 1024),
+                            smem_desc_sw128(xt, 1024, 1024), idS, 0u);
                 }
-                mma_commit(&sm.s_full);
-                mma_commit(&sm.xt_empty);
+                mma_commit_e(&sm.s_full);
+                mma_commit_e(&sm.xt_empty);
                 if (!full_tile) {
-                    mma_commit(&sm.bc_empty[s]);
-                    mma_commit(&sm.x_empty[xs]);
-                    advance(c, plan, sm, p);
+                    mma_commit_e(&sm.bc_empty[s]);
+                    mma_commit_e(&sm.x_empty[xs]);
+                    advance_p(c, plan, sm, p);
                     continue;
                 }
                 const int yb = j % K::kYBuf;
                 const uint32_t ypar = (uint32_t)(j / K::kYBuf) & 1u;
                 // off-diagonal Y_off = C h_prev^T, into the accumulator buffer of this tile
-                if (!wait_bar(&sm.h_full, (uint32_t)j & 1u, sm, p) ||
-                    !wait_bar(&sm.y_empty[yb], ypar ^ 1u, sm, p))
+                if (!wait_warp_p(&sm.h_full, (uint32_t)j & 1u, sm, p) ||
+                    !wait_warp_p(&sm.y_empty[yb], ypar ^ 1u, sm, p))
                     break;
                 tc_fence_after();
                 {
                     const uint32_t cbase = sbase + K::kOffBC + s * K::kBCBytes +
                                            K::kNReg * kTileBytes;
                     const uint32_t ht = sbase + K::kOffHt;
-#pragma unroll 1
-                    for (int kk = 0; kk < NS / 16; ++kk)
-                        mma_f16(tmem + K::kColYoff + yb * kPS,
-                                smem_desc_sw128(cbase + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16,
-                                                1024),
-                                smem_desc_sw128(ht + kk * 2048, 1024, 1024), idYoff, kk > 0);
+#pragma unroll
+                    for (int kb = 0; kb < NS / 128; ++kb)
+                        mma8_ss_e<kStepCols, kStepRows>(
+                            tmem + K::kColYoff + yb * kPS,
+                            smem_desc_sw128(cbase + 2 * kb * kTileBytes, 16, 1024),
+                            smem_desc_sw128(ht + kb * 8 * 2048, 1024, 1024), idYoff, kb > 0);
                 }
-                mma_commit(&sm.h_empty);
-                mma_commit(&sm.bc_empty[s]);   // G, S^T and Y_off have read this B / C stage
+                mma_commit_e(&sm.h_empty);
+                mma_commit_e(&sm.bc_empty[s]);   // G, S^T and Y_off have read this B / C stage
                 // next tile's C B^T while this tile's P is built
                 if (K::kBCStages > 1 && next_full) {
                     if (!issue_G(nt + 1, j + 1)) break;
                     g_ahead = true;
                 }
                 // Y_diag = P X, P read from TMEM
-                if (!wait_bar(&sm.p_full, (uint32_t)j & 1u, sm, p)) break;
+                if (!wait_warp_p(&sm.p_full, (uint32_t)j & 1u, sm, p)) break;
                 tc_fence_after();
                 {
                     const uint32_t xb = sbase + K::kOffX + xs * kTileBytes;
-#pragma unroll 1
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_f16_ts(tmem + K::kColY + yb * kPS, tmem + K::kColP + kk * 8,
-                                   smem_desc_sw128(xb + kk * 2048, 1024, 1024), idYd, kk > 0);
+                    mma8_ts_e<kStepRows>(tmem + K::kColY + yb * kPS, tmem + K::kColP,
+                                         smem_desc_sw128(xb, 1024, 1024), idYd, 0u);
                 }
-                mma_commit(&sm.y_full[yb]);
-                mma_commit(&sm.p_empty);
-                mma_commit(&sm.x_empty[xs]);
+                mma_commit_e(&sm.y_full[yb]);
+                mma_commit_e(&sm.p_empty);
+                mma_commit_e(&sm.x_empty[xs]);
                 if (K::kBCStages == 1 && next_full) {
                     if (!issue_G(nt + 1, j + 1)) break;
                     g_ahead = true;
                 }
                 ++j;
-                advance(c, plan, sm, p);
+                advance_p(c, plan, sm, p);
             }
             // every MMA issued above has completed once this barrier's phase 0 completes
-            mma_commit(&sm.mma_done);
+            mma_commit_e(&sm.mma_done);
             const long long t0 = clock64();
             while (!mbar_try_wait(&sm.mma_done, 0) && clock64() - t0 < p.budget) {
             }
         }
     }
     } else {
-        regs_inc<kRegsCompute>();
+        regs_inc<K::kRegsCompute>();
         // ------------------------------------------------------------- compute warps -----
-        const int w = warp - kWarpC;             // 0..7
+        constexpr int CW = K::kCW;
+        const int w = warp - kWarpC;             // 0 .. 4 kWG - 1
         const int q = warp & 3;                  // TMEM lane quarter
-        const int hsel = w >> 2;                 // column half
+        const int wg = w >> 2;                   // column block
         const int r = q * 32 + lane;             // tile row, and state row inside a 128-block
-        const int c0 = hsel * 32;
+        const int c0 = wg * CW;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        // P column blocks of this warpgroup, balanced over the lane quarters
-        const int jbA = hsel ? 1 : 0, jbB = hsel ? 2 : 3;
         float h[K::kHReg];
-        PendingY pend;
+        PendingY<CW> pend;
         bool have_pend = false;
         // the deferred y epilogue of full tile pj: y = Y_diag + exp(cum) Y_off + D x for this
-        // thread's half row, in two 16-column steps
+        // thread's row and column block, in 16-column steps
         auto epilogue = [&](int pj) -> bool {
             const int yb = pj % K::kYBuf;
             if (!wait_warp(&sm.y_full[yb], (uint32_t)(pj / K::kYBuf) & 1u, sm, p)) return false;
             tc_fence_after();
-            float yd[32], yo[32];
-            tmem_ld32x2(tmem + lane_base + K::kColY + yb * kPS + c0, yd,
-                        tmem + lane_base + K::kColYoff + yb * kPS + c0, yo);
+            float yd[CW], yo[CW];
+            tmem_ld_pair<CW>(tmem + lane_base + K::kColY + yb * kPS + c0, yd,
+                             tmem + lane_base + K::kColYoff + yb * kPS + c0, yo);
 #pragma unroll
-            for (int qc = 0; qc < 2; ++qc) {
+            for (int qc = 0; qc < CW / 16; ++qc) {
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const uint4 xv = pend.x[qc * 2 + cc];
@@ -914,12 +984,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     Dh = p.D ? p.D[uc.h] : 0.f;
                 }
                 if (c.it.init == kInitLookback) {
-                    if (!look_back<NS>(h, p, sm, w, lane, r, c0)) { ok = false; break; }
+                    if (!look_back<NS, CW>(h, p, sm, w, lane, r, c0)) { ok = false; break; }
                 } else {
                     const float* src = (c.it.init == kInitH0 && p.h0)
                                            ? p.h0 + ((int64_t)uc.bh * p.P + (int64_t)uc.ps * kPS) * NS
                                            : nullptr;
-                    h_from<NS>(h, src, r, c0, 0.f, false, false);
+                    h_from<NS, CW>(h, src, r, c0, 0.f, false, false);
                 }
                 if (full_tile) {
                     // h^T for the item's first Y_off, once the previous full tile's Y_off is done
@@ -927,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    ht_write<NS>(h, smem + K::kOffHt, r, hsel);
+                    ht_write<NS, CW>(h, smem + K::kOffHt, r, wg);
                     fence_proxy_async_smem();
                     mbar_arrive(&sm.h_full);
                 }
@@ -938,22 +1008,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             // w o X for the chunk-state GEMM: row r scaled by exp(cum_last - cum_r) dt_r; the raw
             // x row stays in registers for this tile's (deferred) D x term
             if (!wait_warp(&sm.xt_empty, par ^ 1u, sm, p)) { ok = false; break; }
-            uint4 xk[4];
+            uint4 xk[CW / 8];
             {
                 const float wr = sl.w[r];
                 const uint8_t* xrow = smem + K::kOffX + xs * kTileBytes;
                 uint8_t* xtrow = smem + K::kOffXt;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    xk[cc] = *reinterpret_cast<const uint4*>(xrow + sw128_off(r, hsel * 4 + cc));
+                for (int cc = 0; cc < CW / 8; ++cc)
+                    xk[cc] = *reinterpret_cast<const uint4*>(xrow + sw128_off(r, wg * (CW / 8) + cc));
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < CW / 8; ++cc) {
                     const uint32_t in[4] = {xk[cc].x, xk[cc].y, xk[cc].z, xk[cc].w};
                     uint32_t o[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         o[e] = pack_bf16x2(wr * bf16lo_to_f32(in[e]), wr * bf16hi_to_f32(in[e]));
-                    *reinterpret_cast<uint4*>(xtrow + sw128_off(r, hsel * 4 + cc)) =
+                    *reinterpret_cast<uint4*>(xtrow + sw128_off(r, wg * (CW / 8) + cc)) =
                         make_uint4(o[0], o[1], o[2], o[3]);
                 }
             }
@@ -961,15 +1031,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&sm.xt_full);
 
             if (full_tile) {
-                // this warp's two column blocks of P (those above the diagonal stay zero)
+                // this warp's column blocks of P (those above the diagonal stay zero)
                 if (!wait_warp(&sm.g_full, (uint32_t)j & 1u, sm, p)) { ok = false; break; }
                 if (!wait_warp(&sm.p_empty, ((uint32_t)j & 1u) ^ 1u, sm, p)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t tg = tmem + lane_base + K::kColG;
                 const uint32_t tp = tmem + lane_base + K::kColP;
 #pragma unroll 1
-                for (int bi = 0; bi < 2; ++bi) {
-                    const int jb = bi ? jbB : jbA;
+                for (int bi = 0; bi < K::kPB; ++bi) {
+                    const int jb = p_col_block<K::kWG>(wg, bi);
                     if (jb > q) continue;
                     float g[32];
                     tmem_ld32(tg + 32 * jb, g);
@@ -999,15 +1069,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int mb = 0; mb < K::kMB; ++mb) {
-                float sv[32];
-                tmem_ld32(tmem + lane_base + K::kColS + mb * kPS + c0, sv);
+                float sv[CW];
+                tmem_ld_cols<CW>(tmem + lane_base + K::kColS + mb * kPS + c0, sv);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) h[mb * 32 + i] = fmaf(decay, h[mb * 32 + i], sv[i]);
+                for (int i = 0; i < CW; ++i) h[mb * CW + i] = fmaf(decay, h[mb * CW + i], sv[i]);
             }
             tc_fence_before();
             mbar_arrive(&sm.s_empty);
             if (write_ht) {
-                ht_write<NS>(h, smem + K::kOffHt, r, hsel);
+                ht_write<NS, CW>(h, smem + K::kOffHt, r, wg);
                 fence_proxy_async_smem();
                 mbar_arrive(&sm.h_full);
             }
@@ -1023,7 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pend.e = e_r;
                 pend.d = Dh;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) pend.x[cc] = xk[cc];
+                for (int cc = 0; cc < CW / 8; ++cc) pend.x[cc] = xk[cc];
                 have_pend = true;
                 ++j;
             }
@@ -1032,10 +1102,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- end of an item: final state, or publish for the next range
                 if (c.it.fin == kFinFinal) {
                     if (p.hT)
-                        h_to<NS>(h, p.hT + ((int64_t)uc.bh * p.P + (int64_t)uc.ps * kPS) * NS, r,
+                        h_to<NS, CW>(h, p.hT + ((int64_t)uc.bh * p.P + (int64_t)uc.ps * kPS) * NS, r,
                                  c0);
                 } else {
-                    publish<NS>(h, p, w, lane, r, c0, c.it.fin, item_logd);
+                    publish<NS, CW>(h, p, w, lane, r, c0, c.it.fin, item_logd);
                 }
             }
         }
@@ -1135,7 +1205,7 @@ int launch_ns(const ScanArgs& a) {
     if (cudaFuncSetAttribute(ssd_tc_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return SSD_ERR_CUDA;
-    ssd_tc_kernel<NS><<<(unsigned)p.n_ctas, kThreads, smem, a.stream>>>(tmX, tmB, tmC, p);
+    ssd_tc_kernel<NS><<<(unsigned)p.n_ctas, Cfg<NS>::kThreads, smem, a.stream>>>(tmX, tmB, tmC, p);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

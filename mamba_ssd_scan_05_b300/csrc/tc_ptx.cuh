@@ -124,6 +124,110 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
         : "memory");
 }
 
+// Forms of the three above for a whole warp in converged control flow: one elected lane (the
+// same lane every time, so its commits track its own MMAs) issues the instruction.  Issuing
+// from converged code keeps the operands in the warp-uniform datapath.
+__device__ __forceinline__ void mma_f16_e(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_f16_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_e(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// Descriptor offsets (16-byte units) of the K steps of a K = 128 GEMM over 128-byte swizzled
+// tiles: kStepRows for an operand whose K runs down the rows (16 rows of 128 bytes per step),
+// kStepCols for a K-major operand (32 bytes per step inside a 64-column region of 16 KB).
+enum : int { kStepRows = 0, kStepCols = 1 };
+__host__ __device__ constexpr long long desc_step(int pattern, int k) {
+    return pattern == kStepRows ? k * 128 : (k >> 2) * 1024 + (k & 3) * 2;
+}
+
+// One K = 128 GEMM (8 K-steps of 16) issued by a whole warp in converged control flow: one
+// elected lane issues the 8 MMAs back to back with descriptors base + compile-time offsets.
+// The first step accumulates when `accumulate` is nonzero; the rest always accumulate.
+template <int PA, int PB>
+__device__ __forceinline__ void mma8_ss_e(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 r;\n\t.reg .b64 a, b;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, %3, %3;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %12;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.s64 a, %1, %6;\n\tadd.s64 b, %2, %13;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %14;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.s64 a, %1, %8;\n\tadd.s64 b, %2, %15;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %16;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.s64 a, %1, %10;\n\tadd.s64 b, %2, %17;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.s64 a, %1, %11;\n\tadd.s64 b, %2, %18;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+        "}\n" ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate),
+        "n"(desc_step(PA, 1)), "n"(desc_step(PA, 2)), "n"(desc_step(PA, 3)), "n"(desc_step(PA, 4)),
+        "n"(desc_step(PA, 5)), "n"(desc_step(PA, 6)), "n"(desc_step(PA, 7)),
+        "n"(desc_step(PB, 1)), "n"(desc_step(PB, 2)), "n"(desc_step(PB, 3)), "n"(desc_step(PB, 4)),
+        "n"(desc_step(PB, 5)), "n"(desc_step(PB, 6)), "n"(desc_step(PB, 7))
+        : "memory");
+}
+
+// The same with the A operand in TMEM (8 columns per K step from a_tmem).
+template <int PB>
+__device__ __forceinline__ void mma8_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 r, ta;\n\t.reg .b64 b;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, %3, %3;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.u32 ta, %1, 8;\n\tadd.s64 b, %2, %5;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
+        "add.u32 ta, %1, 16;\n\tadd.s64 b, %2, %6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
+        "add.u32 ta, %1, 24;\n\tadd.s64 b, %2, %7;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
+        "add.u32 ta, %1, 32;\n\tadd.s64 b, %2, %8;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
+        "add.u32 ta, %1, 40;\n\tadd.s64 b, %2, %9;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
+        "add.u32 ta, %1, 48;\n\tadd.s64 b, %2, %10;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
+        "add.u32 ta, %1, 56;\n\tadd.s64 b, %2, %11;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
+        "}\n" ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate),
+        "n"(desc_step(PB, 1)), "n"(desc_step(PB, 2)), "n"(desc_step(PB, 3)), "n"(desc_step(PB, 4)),
+        "n"(desc_step(PB, 5)), "n"(desc_step(PB, 6)), "n"(desc_step(PB, 7))
+        : "memory");
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn: 0 = K-major operand, 1 = MN-major operand.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
@@ -168,6 +272,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane, waited for.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Two loads of 32 consecutive 32-bit TMEM columns each, one wait for both.
