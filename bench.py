@@ -66,10 +66,18 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_sha() -> str:
+# Source files each profiled kernel is built from (a traffic record is valid for these bytes).
+KERNEL_SOURCES = {
+    "ssd_tc_kernel": ("tc.cu", "tc_ptx.cuh", "common.cuh"),
+    "step_kernel_vec": ("step.cu", "common.cuh"),
+    "chunk_output_kernel": ("chunked.cu", "common.cuh"),
+}
+
+
+def kernel_source_sha(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mamba_ssd_scan_05_b300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in KERNEL_SOURCES.get(kernel, ()):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
@@ -82,7 +90,7 @@ def committed_traffic(kernel: str, workload: str):
         with open(path) as f:
             d = json.load(f)
         e = d[f"{kernel}|{workload}"]
-        if e.get("source_sha") != kernel_source_sha():
+        if e.get("source_sha") != kernel_source_sha(kernel):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -232,6 +240,119 @@ def run_reference(args, w, ws, rank):
     return 0
 
 
+STEP_METRIC = "SSD recurrent decode step tokens/s on 1 B300; % of roofline (HBM)"
+
+
+def step_bytes(w) -> int:
+    """Algorithmic bytes of one decode step: the float32 state read and written once, plus the
+    step's inputs and y."""
+    eb = 4 if w.dtype == "f32" else 2
+    b, H, P, N, G = w.batch, w.nheads, w.headdim, w.dstate, w.ngroups
+    return (2 * 4 * b * H * P * N + eb * (2 * b * H * P + b * H + 2 * b * G * N) + 4 * 2 * H)
+
+
+def run_step(args, ws, rank, local):
+    """The recurrent step (ssd_step_fwd) on the decode workload, state updated in place."""
+    import torch
+    import mamba_ssd_scan_05_b300 as m
+    from mamba_ssd_scan_05_b300 import workloads
+    w = workloads.DECODE[0]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = workloads.make_inputs(w)
+    d = {k: v.to(dev) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    state = d["h0"]      # 335 MB of float32 state, updated in place: larger than L2 every step
+
+    def step():
+        m.ssd_step_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], state, y=y)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    # the timed calls replay a CUDA graph of one call, so host-side argument handling does not
+    # leave the GPU idle between calls
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        graph.replay()
+        ends[i].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    total_ms = ev0.elapsed_time(ev1)
+    call_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms_per_step = total_ms / args.steps
+    value = w.batch / (ms_per_step / 1e3)
+
+    # end to end through the public call: this step's token inputs from pinned host memory,
+    # the step (state resident on the device), y back to pinned host memory
+    e2e = None
+    if args.e2e_steps > 0:
+        names = ("x", "dt", "B", "C")
+        pinned = {k: inp[k].pin_memory() for k in names}
+        y_h = torch.empty_like(pinned["x"], pin_memory=True)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            for k in names:
+                d[k].copy_(pinned[k], non_blocking=True)
+            step()
+            y_h.copy_(y, non_blocking=True)
+            torch.cuda.synchronize(dev)
+        t_e2e = time.perf_counter() - t0
+        e2e = {"value": w.batch * args.e2e_steps / t_e2e, "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in pinned.values()),
+               "d2h_bytes_per_step": y_h.numel() * y_h.element_size()}
+    if rank != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    nbytes = step_bytes(w)
+    avg_call_s = statistics.mean(call_ms) / 1e3
+    achieved = nbytes / avg_call_s / 1e9
+    kernel = "step_kernel_vec"
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": committed_traffic(kernel, w.name),
+                "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
+                "t_roof_us": 1e6 * nbytes / (peaks["hbm_gbs"] * 1e9),
+                "algorithmic_bytes": nbytes, "kernel": kernel,
+                "timed": "ssd_step_fwd call (CUDA graph replay)"}
+    cpu = None
+    if not args.no_cpu_baseline:
+        r, used, desc, _ = oracle_sample_rate(w, inp, budget_s=4.0)
+        cpu = {"value": r, "unit": "tokens/s", "cores": used, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": STEP_METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": workload_config(w, {"l2": f"state of {4 * w.batch * w.nheads * w.headdim * w.dstate / 1e6:.0f} MB updated in place (larger than L2)",
+                                      "op": "step", "parallelism": "replicas x1"}),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": args.steps, "clocks": sampler.summary(wall0, wall1),
+        "per_call_ms": {"median": statistics.median(call_ms), "min": min(call_ms),
+                        "max": max(call_ms)},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -243,9 +364,16 @@ def main():
     ap.add_argument("--path", type=int, default=-1, help="kernel family (-1 auto, 0 chunked, 1 tc)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["scan", "step"], default="scan",
+                    help="scan: the forward scan (default); step: the recurrent decode step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.op == "step":
+        ws, rank, local = dist_setup()
+        if args.impl == "reference" or ws > 1:
+            raise SystemExit("--op step: our arm on one GPU only")
+        return run_step(args, ws, rank, local)
 
     from mamba_ssd_scan_05_b300 import workloads
     w = workloads.WORKLOADS[args.workload]
@@ -289,12 +417,26 @@ def main():
                        chunk_size=w.chunk, path=args.path, y=d["y"], final_state=d["hT"],
                        workspace=workspace)
 
-    stream = torch.cuda.current_stream(dev)
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
     if m.ssd_scan_get_status(workspace) != 0:
         raise SystemExit("device status error during warm-up")
+    # the timed calls replay one CUDA graph per input set (each graph holds one ssd_scan_fwd
+    # call: the status-word memset and the kernels), so host-side argument handling does not
+    # leave the GPU idle between calls
+    graphs = []
+    for i in range(n_sets):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(i)
+        graphs.append(g)
+    for i in range(args.warmup):
+        graphs[i % n_sets].replay()
+    torch.cuda.synchronize(dev)
+    if m.ssd_scan_get_status(workspace) != 0:
+        raise SystemExit("device status error during warm-up")
+    stream = torch.cuda.current_stream(dev)
 
     sampler = ClockSampler(local).start()
     time.sleep(0.3)
@@ -309,7 +451,7 @@ def main():
     ev0.record(stream)
     for i in range(args.steps):
         starts[i].record(stream)
-        step(args.warmup + i)
+        graphs[(args.warmup + i) % n_sets].replay()
         ends[i].record(stream)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
@@ -382,7 +524,8 @@ def main():
                 "t_roof_us": 1e6 * max(t_hbm, t_tc),
                 "roof_frac": max(t_hbm, t_tc) / avg_call_s,
                 "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-                "kernel": kernel, "timed": "whole ssd_scan_fwd call (status memset + kernels)"}
+                "kernel": kernel,
+                "timed": "whole ssd_scan_fwd call (status memset + kernels), CUDA graph replay"}
 
     cpu = None
     if not args.no_cpu_baseline and ws >= 1:

@@ -164,6 +164,35 @@ int ssd_scan_fwd_noalloc(const ssd_dims* dims,
                          const float* initial_state, int chunk_size,
                          void* y, float* final_state, void* stream);
 
+/*
+ * ssd_step_fwd -- one recurrent step per (batch row, head): the scan above for a single token,
+ * for decoding, where tokens arrive one at a time and the state lives between calls.
+ *
+ *     state[b,h] <- exp(dt[b,h] * A[h]) * state[b,h] + dt[b,h] * x[b,h] B[b,g]^T
+ *     y[b,h,p]    = sum_n C[b,g,n] * state[b,h][p][n] + D[h] * x[b,h,p]     (g = h / (H / G))
+ *
+ * i.e. ssd_scan_fwd with seqlen 1, initial_state = state_in and final_state = state_out (the
+ * recurrent mode: waylandz.com chapter 32, section 32.2.4; the recurrence: youngju.dev article,
+ * section "LTIからSelectionへの切り替え").
+ *
+ *   - dims.seqlen must be 1; the layouts are those above with L = 1: x [batch, 1, nheads,
+ *     headdim], dt [batch, 1, nheads], B, C [batch, 1, ngroups, dstate] (dtype T), y [batch, 1,
+ *     nheads, headdim] (T, written).  Any headdim and dstate.
+ *   - state_in, state_out: [batch, nheads, headdim, dstate] float32, device memory.  state_in
+ *     NULL means a zero state; state_out is required and is written completely.  state_out may
+ *     equal state_in (update in place); otherwise the two must not overlap.
+ *   - D may be NULL (no skip term).  Alignment as for ssd_scan_fwd (x, dt, B, C, y 16 bytes;
+ *     A, D and the states 4 bytes).
+ *   - Needs no workspace and allocates nothing.  Enqueued on `stream`.
+ *   - Returns SSD_OK once enqueued; SSD_ERR_INVALID for bad arguments (including seqlen != 1 or
+ *     partially overlapping states), SSD_ERR_UNSUPPORTED if batch * nheads exceeds 2^31 - 1,
+ *     SSD_ERR_CUDA if the launch fails.  Nothing is enqueued on an error.
+ */
+int ssd_step_fwd(const ssd_dims* dims,
+                 const void* x, const void* dt, const float* A,
+                 const void* B, const void* C, const float* D,
+                 const float* state_in, float* state_out, void* y, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word of `workspace` (the first
  * 4 bytes).  Returns SSD_OK, SSD_ERR_TIMEOUT if a bounded device wait gave up in a call that
  * used this workspace, or SSD_ERR_CUDA if synchronisation or the read failed. */

@@ -1,6 +1,7 @@
 """Mamba-2 SSD forward scan for NVIDIA B300 (sm_103a).
 
 Per head: h_t = exp(dt_t A) h_{t-1} + dt_t x_t B_t^T,  y_t = C_t^T h_t + D x_t.
+``ssd_step_fwd`` is the same recurrence for one token per sequence (decoding).
 The computation lives in ``libssd_scan.so`` (C ABI in ``include/ssd_scan.h``); this package is
 its ctypes binding plus the seeded synthetic workloads (``workloads``).
 """
@@ -24,4 +25,5 @@ from ._binding import (  # noqa: F401
     ssd_scan_strerror,
     ssd_scan_version,
     ssd_scan_workspace_bytes,
+    ssd_step_fwd,
 )

@@ -63,6 +63,8 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_scan_host_arena_bytes.restype = sz
         lib.ssd_scan_fwd_host.argtypes = fwd_args
         lib.ssd_scan_fwd_host.restype = i32
+        lib.ssd_step_fwd.argtypes = [dims_p, vp, vp, fp, vp, vp, fp, fp, fp, vp, vp]
+        lib.ssd_step_fwd.restype = i32
         lib.ssd_scan_get_status.argtypes = [vp, vp]
         lib.ssd_scan_get_status.restype = i32
         lib.ssd_scan_strerror.argtypes = [i32]
@@ -168,6 +170,40 @@ def ssd_scan_fwd(x, dt, A, B, C, D=None, initial_state=None, chunk_size: int = 2
     if rc != SSD_OK:
         raise SSDError(rc, "ssd_scan_fwd")
     return y, final_state
+
+
+def ssd_step_fwd(x, dt, A, B, C, D=None, state=None, state_out=None, y=None):
+    """One recurrent step (a single token per sequence) on x's CUDA device.
+
+    x [b,1,H,P] or [b,H,P]; dt [b,1,H] or [b,H]; B, C [b,1,G,N] or [b,G,N]; A, D float32 [H];
+    state float32 [b,H,P,N] or None (zeros).  The new state goes to ``state_out``: by default
+    ``state`` itself (updated in place), or a new tensor when ``state`` is None.  Returns
+    (y, state_out) with y shaped like x.  Enqueued on torch's current stream.
+    """
+    squeeze = x.dim() == 3
+    if squeeze:
+        x, dt, B, C = x.unsqueeze(1), dt.unsqueeze(1), B.unsqueeze(1), C.unsqueeze(1)
+    _check_inputs(x, dt, A, B, C, D, state)
+    if x.shape[1] != 1:
+        raise ValueError("ssd_step_fwd: one token per sequence (seqlen 1)")
+    if not x.is_cuda:
+        raise ValueError("ssd_step_fwd: tensors must be on a CUDA device")
+    b, _, H, P = x.shape
+    N = B.shape[3]
+    if state_out is None:
+        state_out = state if state is not None else torch.empty(
+            (b, H, P, N), dtype=torch.float32, device=x.device)
+    elif (state_out.shape != (b, H, P, N) or state_out.dtype != torch.float32
+          or not state_out.is_contiguous()):
+        raise ValueError("ssd_step_fwd: state_out must be contiguous float32 [b,H,P,N]")
+    if y is None:
+        y = torch.empty_like(x)
+    rc = load_library().ssd_step_fwd(ctypes.byref(make_dims(x, B)), _ptr(x), _ptr(dt), _ptr(A),
+                                     _ptr(B), _ptr(C), _ptr(D), _ptr(state), _ptr(state_out),
+                                     _ptr(y), _stream_handle(x.device))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_step_fwd")
+    return (y.squeeze(1) if squeeze else y), state_out
 
 
 def ssd_scan_get_status(workspace, device=None) -> int:

@@ -56,6 +56,25 @@ size_t chunked_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t P, int64
 bool chunked_supports(int64_t P, int64_t N, int Q);
 int chunked_launch(const ScanArgs& a);
 
+// Arguments of one recurrent step (ssd_step_fwd), after validation.
+struct StepArgs {
+    int64_t batch, nheads, headdim, dstate, ngroups;
+    int32_t dtype;
+    const void* x;             // [batch, nheads, headdim]
+    const void* dt;            // [batch, nheads]
+    const float* A;
+    const void* B;             // [batch, ngroups, dstate]
+    const void* C;
+    const float* D;            // may be null
+    const float* s_in;         // [batch, nheads, headdim, dstate]; null = zeros; may equal s_out
+    float* s_out;
+    void* y;                   // [batch, nheads, headdim]
+    cudaStream_t stream;
+};
+
+// Recurrent step (step.cu).
+int step_launch(const StepArgs& a);
+
 // Tensor-core path (tc.cu).
 size_t tc_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t P, int64_t N, int Q);
 bool tc_supports(int32_t dtype, int64_t P, int64_t N, int Q);

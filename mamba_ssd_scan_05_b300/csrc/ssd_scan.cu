@@ -185,6 +185,35 @@ int ssd_scan_fwd_host(const ssd_dims* dims, const void* x, const void* dt, const
     return SSD_OK;
 }
 
+int ssd_step_fwd(const ssd_dims* dims, const void* x, const void* dt, const float* A,
+                 const void* B, const void* C, const float* D, const float* state_in,
+                 float* state_out, void* y, void* stream) {
+    if (!dims || dims->seqlen != 1) return SSD_ERR_INVALID;
+    const int rc = check_dims(dims, 1);
+    if (rc != SSD_OK) return rc;
+    if (!x || !dt || !A || !B || !C || !y || !state_out) return SSD_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(B, 16) || !aligned(C, 16) ||
+        !aligned(y, 16) || !aligned(A, 4) || !aligned(D, 4) || !aligned(state_in, 4) ||
+        !aligned(state_out, 4))
+        return SSD_ERR_INVALID;
+    // the state is updated in place or copied to a separate buffer, never a partial overlap
+    const size_t sb = sizeof(float) * (size_t)(dims->batch * dims->nheads * dims->headdim *
+                                               dims->dstate);
+    if (state_in && state_in != state_out) {
+        const uintptr_t i0 = reinterpret_cast<uintptr_t>(state_in);
+        const uintptr_t o0 = reinterpret_cast<uintptr_t>(state_out);
+        if (i0 < o0 + sb && o0 < i0 + sb) return SSD_ERR_INVALID;
+    }
+    if (dims->batch * dims->nheads > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
+    StepArgs a;
+    a.batch = dims->batch; a.nheads = dims->nheads; a.headdim = dims->headdim;
+    a.dstate = dims->dstate; a.ngroups = dims->ngroups; a.dtype = dims->dtype;
+    a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D;
+    a.s_in = state_in; a.s_out = state_out; a.y = y;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return step_launch(a);
+}
+
 int ssd_scan_get_status(void* workspace, void* stream) {
     if (!workspace) return SSD_ERR_INVALID;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -73,6 +73,15 @@ WORKLOADS = {
 }
 
 
+# Decoding: one token per sequence through the recurrent step (ssd_step_fwd), on the
+# 2.7B-shaped layer's heads with a batch of 128 sequences (a float32 state of 335 MB, larger
+# than L2), drawn from the same distributions with a random entering state.
+DECODE = {
+    0: Workload("decode-2.7b-b128", 128, 1, 80, 64, 128, 1, 1, "bf16", d_mode="normal",
+                h0_mode="normal", seed=1100),
+}
+
+
 def _randn(gen, shape, std, block_axis=1):
     """fp32 normal draws, taken in fixed token blocks along ``block_axis``."""
     if len(shape) <= block_axis or shape[block_axis] <= _BLOCK_TOKENS:

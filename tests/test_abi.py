@@ -115,3 +115,23 @@ def test_host_arena_bytes(lib):
     need = m.ssd_scan_host_arena_bytes(d, 64)
     assert need > 2 * (64 * 2 * 32 * 4)
     assert m.ssd_scan_host_arena_bytes(dims(H=6, G=4), 64) == 0
+
+
+def test_step_argument_checks_need_no_gpu(lib):
+    """ssd_step_fwd rejects bad arguments before it touches the GPU."""
+    import ctypes
+    import mamba_ssd_scan_05_b300 as m
+    p = ctypes.c_void_p(1 << 20)            # never dereferenced: the checks return first
+    q = ctypes.c_void_p((1 << 20) + 4096)
+    def call(d, x=p, dt=p, A=p, B=p, C=p, D=None, s_in=None, s_out=q, y=p):
+        return lib.ssd_step_fwd(ctypes.byref(d), x, dt, A, B, C, D, s_in, s_out, y, None)
+    assert call(dims(L=2)) == 1
+    assert call(dims(L=0)) == 1
+    assert call(dims(L=1), x=None) == 1
+    assert call(dims(L=1), s_out=None) == 1
+    assert call(dims(L=1, H=6, G=4)) == 1
+    assert call(dims(L=1, dtype=5)) == 1
+    assert call(dims(L=1), x=ctypes.c_void_p((1 << 20) + 8)) == 1          # misaligned
+    # states overlapping without being the same buffer
+    assert call(dims(L=1, b=1, H=1, P=4, N=4), s_in=ctypes.c_void_p(1 << 20),
+                s_out=ctypes.c_void_p((1 << 20) + 16)) == 1
