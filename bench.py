@@ -70,6 +70,8 @@ def load_peaks():
 KERNEL_SOURCES = {
     "ssd_tc_kernel": ("tc.cu", "tc_ptx.cuh", "common.cuh"),
     "step_kernel_vec": ("step.cu", "common.cuh"),
+    "conv_kernel": ("block.cu", "common.cuh"),
+    "norm_kernel": ("block.cu", "common.cuh"),
     "chunk_output_kernel": ("chunked.cu", "common.cuh"),
 }
 
@@ -353,6 +355,138 @@ def run_step(args, ws, rank, local):
     return 0
 
 
+def run_block(args, op, local):
+    """The block steps around the scan: causal conv1d + SiLU (op conv) or gated RMSNorm (op
+    norm) on the 2.7B-shaped layer's tensors.  Both read each input once and write each output
+    once (HBM-bound); the timed calls replay a CUDA graph of one call."""
+    import torch
+    import mamba_ssd_scan_05_b300 as m
+    from mamba_ssd_scan_05_b300 import workloads
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if op == "conv":
+        c = workloads.CONV
+        inp = workloads.make_conv_inputs(c["batch"], c["seqlen"], c["channels"], c["width"],
+                                         c["dtype"], seed=c["seed"])
+        d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+        out = torch.empty_like(d["x"])
+        st = torch.empty((c["batch"], c["width"] - 1, c["channels"]), dtype=d["x"].dtype,
+                         device=dev)
+
+        def call():
+            m.ssd_causal_conv1d_fwd(d["x"], d["weight"], d["bias"], out=out, state_out=st,
+                                    return_state=True)
+        eb = d["x"].element_size()
+        n_el = c["batch"] * c["seqlen"] * c["channels"]
+        nbytes = 2 * eb * n_el + 4 * c["channels"] * (c["width"] + 1) + eb * st.numel()
+        tokens = c["batch"] * c["seqlen"]
+        kernel, name = "conv_kernel", "conv1d-2.7b-xBC"
+        cfg = dict(c, workload=f"{name}: b={c['batch']} L={c['seqlen']} C={c['channels']} "
+                               f"K={c['width']} {c['dtype']}")
+        metric = "causal conv1d + SiLU tokens/s on 1 B300; % of roofline (HBM)"
+    else:
+        n = workloads.NORM
+        inp = workloads.make_norm_inputs(n["rows"], n["dim"], n["dtype"], seed=n["seed"])
+        d = {k: v.to(dev) for k, v in inp.items()}
+        out = torch.empty_like(d["y"])
+
+        def call():
+            m.ssd_gated_rmsnorm_fwd(d["y"], d["z"], d["weight"], group_size=n["group_size"],
+                                    out=out)
+        eb = d["y"].element_size()
+        nbytes = 3 * eb * n["rows"] * n["dim"] + 4 * n["dim"]
+        tokens = n["rows"]
+        kernel, name = "norm_kernel", "gatednorm-2.7b"
+        cfg = dict(n, workload=f"{name}: rows={n['rows']} dim={n['dim']} "
+                               f"group={n['group_size']} {n['dtype']}")
+        metric = "gated RMSNorm tokens/s on 1 B300; % of roofline (HBM)"
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        graph.replay()
+        ends[i].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    total_ms = ev0.elapsed_time(ev1)
+    call_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms_per_step = total_ms / args.steps
+    # end to end: the inputs from pinned host memory, the call, the output back, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        names = [k for k, v in inp.items() if v is not None and v.dim() > 1 and k != "weight"]
+        pinned = {k: inp[k].pin_memory() for k in names}
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            for k in names:
+                d[k].copy_(pinned[k], non_blocking=True)
+            call()
+            out_h.copy_(out, non_blocking=True)
+            torch.cuda.synchronize(dev)
+        t_e2e = time.perf_counter() - t0
+        e2e = {"value": tokens * args.e2e_steps / t_e2e, "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in pinned.values()),
+               "d2h_bytes_per_step": out_h.numel() * out_h.element_size()}
+    peaks, peak_src = load_peaks()
+    avg_call_s = statistics.mean(call_ms) / 1e3
+    achieved = nbytes / avg_call_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": committed_traffic(kernel, name),
+                "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
+                "t_roof_us": 1e6 * nbytes / (peaks["hbm_gbs"] * 1e9), "algorithmic_bytes": nbytes,
+                "kernel": kernel, "timed": f"one call (CUDA graph replay)"}
+    cpu = None
+    if not args.no_cpu_baseline:
+        from oracle import block
+        k = 256 if op == "conv" else 512
+        t0 = time.perf_counter()
+        if op == "conv":
+            block.causal_conv1d(inp["x"][:, :k], inp["weight"], inp["bias"])
+            done = inp["x"].shape[0] * k
+        else:
+            block.gated_rmsnorm(inp["y"][:k], inp["z"][:k], inp["weight"], 1e-5,
+                                workloads.NORM["group_size"])
+            done = k
+        dt_s = time.perf_counter() - t0
+        cpu = {"value": done / dt_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {k} tokens (of every batch row for conv), numpy float64"}
+    line = {
+        "metric": metric, "value": tokens / (ms_per_step / 1e3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg["dtype"], "data": "synthetic",
+        "config": dict(cfg, op=op, l2=f"{nbytes / 1e6:.0f} MB moved per call (larger than L2)",
+                       parallelism="replicas x1"),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+        "clocks": sampler.summary(wall0, wall1),
+        "per_call_ms": {"median": statistics.median(call_ms), "min": min(call_ms),
+                        "max": max(call_ms)},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -364,16 +498,19 @@ def main():
     ap.add_argument("--path", type=int, default=-1, help="kernel family (-1 auto, 0 chunked, 1 tc)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["scan", "step"], default="scan",
-                    help="scan: the forward scan (default); step: the recurrent decode step")
+    ap.add_argument("--op", choices=["scan", "step", "conv", "norm"], default="scan",
+                    help="scan: the forward scan (default); step: the recurrent decode step; "
+                         "conv / norm: the block steps before / after the scan")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.op == "step":
+    if args.op != "scan":
         ws, rank, local = dist_setup()
         if args.impl == "reference" or ws > 1:
-            raise SystemExit("--op step: our arm on one GPU only")
-        return run_step(args, ws, rank, local)
+            raise SystemExit(f"--op {args.op}: our arm on one GPU only")
+        if args.op == "step":
+            return run_step(args, ws, rank, local)
+        return run_block(args, args.op, local)
 
     from mamba_ssd_scan_05_b300 import workloads
     w = workloads.WORKLOADS[args.workload]

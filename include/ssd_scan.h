@@ -193,6 +193,54 @@ int ssd_step_fwd(const ssd_dims* dims,
                  const void* B, const void* C, const float* D,
                  const float* state_in, float* state_out, void* y, void* stream);
 
+/*
+ * ssd_causal_conv1d_fwd -- the depthwise causal convolution and SiLU that produce the scan's
+ * inputs in a Mamba block (youngju.dev "Mamba / selective SSM" article, the Mamba block listing:
+ * a depthwise Conv1d of width d_conv with padding d_conv - 1, cut to the first L outputs, then
+ * SiLU; Qiita "Mamba-2 / SSD" article, section 5.1: the causal-conv1d step before the scan).
+ * Per batch row b, token t and channel c, with K = width:
+ *
+ *     out[b,t,c] = silu(bias[c] + sum_{k<K} weight[c,k] * x[b, t-(K-1)+k, c])
+ *
+ * where inputs before t = 0 come from state_in (zeros when NULL).  silu = 0 skips the SiLU.
+ *
+ *   - x, out:       [batch, seqlen, channels]  T (dtype)     device memory
+ *   - weight:       [channels, width]          float32
+ *   - bias:         [channels]                 float32, or NULL (no bias)
+ *   - state_in:     [batch, width - 1, channels] T, or NULL: the width - 1 inputs before x
+ *   - state_out:    [batch, width - 1, channels] T, or NULL (not written): the last width - 1
+ *                   inputs of state_in ++ x, so the next call continues the sequence
+ *   - 1 <= width <= 8, batch <= 65535, seqlen <= 2^21 - 32.  Element alignment suffices;
+ *     16-byte aligned buffers with channels % (16 / sizeof(T)) == 0 take the vector path.
+ *   - No output may overlap an input, and state_out may not overlap out (SSD_ERR_INVALID).
+ *   - Needs no workspace; enqueued on `stream`.  Returns SSD_OK, SSD_ERR_INVALID,
+ *     SSD_ERR_UNSUPPORTED (sizes beyond the grid limits) or SSD_ERR_CUDA.
+ */
+int ssd_causal_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t channels, int width,
+                          int32_t dtype, const void* x, const float* weight, const float* bias,
+                          const void* state_in, void* state_out, int silu, void* out,
+                          void* stream);
+
+/*
+ * ssd_gated_rmsnorm_fwd -- the step after the scan, y = rmsnorm(y) * silu(z) (Qiita "Mamba-2 /
+ * SSD" article, section 4.2, step 4), per row over groups of group_size features:
+ *
+ *     out[r,i] = y[r,i] / sqrt(mean_{j in group(i)} y[r,j]^2 + eps) * weight[i] * silu(z[r,i])
+ *
+ *   - y, z, out: [rows, dim] T (for the scan's y: rows = batch * seqlen, dim = nheads * headdim)
+ *   - z NULL: no gate.  weight: [dim] float32, or NULL (ones).  eps >= 0 (the pages give no
+ *     value; 1e-5 is the binding's default).  group_size divides dim (dim: one group per row).
+ *   - dim / group_size <= 12288, rows <= 2^31 - 1 (else SSD_ERR_UNSUPPORTED).
+ *   - out may equal y or z (each element is read before it is written by the same thread);
+ *     element alignment suffices, 16-byte alignment with group_size % (16 / sizeof(T)) == 0
+ *     takes the vector path.
+ *   - Needs no workspace; enqueued on `stream`.  Returns SSD_OK, SSD_ERR_INVALID,
+ *     SSD_ERR_UNSUPPORTED or SSD_ERR_CUDA.
+ */
+int ssd_gated_rmsnorm_fwd(int64_t rows, int64_t dim, int64_t group_size, int32_t dtype,
+                          const void* y, const void* z, const float* weight, float eps,
+                          void* out, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word of `workspace` (the first
  * 4 bytes).  Returns SSD_OK, SSD_ERR_TIMEOUT if a bounded device wait gave up in a call that
  * used this workspace, or SSD_ERR_CUDA if synchronisation or the read failed. */

@@ -1,7 +1,9 @@
 """Mamba-2 SSD forward scan for NVIDIA B300 (sm_103a).
 
 Per head: h_t = exp(dt_t A) h_{t-1} + dt_t x_t B_t^T,  y_t = C_t^T h_t + D x_t.
-``ssd_step_fwd`` is the same recurrence for one token per sequence (decoding).
+``ssd_step_fwd`` is the same recurrence for one token per sequence (decoding);
+``ssd_causal_conv1d_fwd`` and ``ssd_gated_rmsnorm_fwd`` are the block's steps before and after
+the scan.
 The computation lives in ``libssd_scan.so`` (C ABI in ``include/ssd_scan.h``); this package is
 its ctypes binding plus the seeded synthetic workloads (``workloads``).
 """
@@ -15,6 +17,8 @@ from ._binding import (  # noqa: F401
     SSD_PATH_TC,
     SSDError,
     load_library,
+    ssd_causal_conv1d_fwd,
+    ssd_gated_rmsnorm_fwd,
     make_dims,
     ssd_dims,
     ssd_scan_fwd,

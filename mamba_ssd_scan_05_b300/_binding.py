@@ -65,6 +65,13 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_scan_fwd_host.restype = i32
         lib.ssd_step_fwd.argtypes = [dims_p, vp, vp, fp, vp, vp, fp, fp, fp, vp, vp]
         lib.ssd_step_fwd.restype = i32
+        i64 = ctypes.c_int64
+        lib.ssd_causal_conv1d_fwd.argtypes = [i64, i64, i64, i32, i32, vp, fp, fp, vp, vp, i32,
+                                              vp, vp]
+        lib.ssd_causal_conv1d_fwd.restype = i32
+        lib.ssd_gated_rmsnorm_fwd.argtypes = [i64, i64, i64, i32, vp, vp, fp, ctypes.c_float,
+                                              vp, vp]
+        lib.ssd_gated_rmsnorm_fwd.restype = i32
         lib.ssd_scan_get_status.argtypes = [vp, vp]
         lib.ssd_scan_get_status.restype = i32
         lib.ssd_scan_strerror.argtypes = [i32]
@@ -204,6 +211,60 @@ def ssd_step_fwd(x, dt, A, B, C, D=None, state=None, state_out=None, y=None):
     if rc != SSD_OK:
         raise SSDError(rc, "ssd_step_fwd")
     return (y.squeeze(1) if squeeze else y), state_out
+
+
+def ssd_causal_conv1d_fwd(x, weight, bias=None, state=None, silu: bool = True,
+                          return_state: bool = False, out=None, state_out=None):
+    """Depthwise causal conv1d (+ SiLU) over x [b, L, C] on its CUDA device.
+
+    weight float32 [C, K] (K <= 8), bias float32 [C] or None, state [b, K-1, C] (x's dtype) or
+    None (zeros).  Returns out [b, L, C], or (out, state_out) with ``return_state``.
+    """
+    if x.dim() != 3 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("ssd_causal_conv1d_fwd: x must be a contiguous CUDA tensor [b, L, C]")
+    b, L, C = x.shape
+    if weight.dim() != 2 or weight.shape[0] != C or weight.dtype != torch.float32:
+        raise ValueError("ssd_causal_conv1d_fwd: weight must be float32 [C, K]")
+    K = weight.shape[1]
+    if bias is not None and (bias.shape != (C,) or bias.dtype != torch.float32):
+        raise ValueError("ssd_causal_conv1d_fwd: bias must be float32 [C]")
+    if state is not None and (state.shape != (b, K - 1, C) or state.dtype != x.dtype):
+        raise ValueError("ssd_causal_conv1d_fwd: state must be [b, K-1, C] of x's dtype")
+    for t in (weight, bias, state):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("ssd_causal_conv1d_fwd: tensors must be contiguous")
+    if out is None:
+        out = torch.empty_like(x)
+    if return_state and state_out is None:
+        state_out = torch.empty((b, K - 1, C), dtype=x.dtype, device=x.device)
+    rc = load_library().ssd_causal_conv1d_fwd(b, L, C, K, _dtype_code(x.dtype), _ptr(x),
+                                              _ptr(weight), _ptr(bias), _ptr(state),
+                                              _ptr(state_out), int(bool(silu)), _ptr(out),
+                                              _stream_handle(x.device))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_causal_conv1d_fwd")
+    return (out, state_out) if return_state else out
+
+
+def ssd_gated_rmsnorm_fwd(y, z=None, weight=None, eps: float = 1e-5, group_size=None, out=None):
+    """rmsnorm(y) * weight * silu(z) over the last dimension (in groups of ``group_size``)."""
+    if not y.is_cuda or not y.is_contiguous():
+        raise ValueError("ssd_gated_rmsnorm_fwd: y must be a contiguous CUDA tensor")
+    D = y.shape[-1]
+    rows = y.numel() // D if D else 0
+    if z is not None and (z.shape != y.shape or z.dtype != y.dtype or not z.is_contiguous()):
+        raise ValueError("ssd_gated_rmsnorm_fwd: z must match y")
+    if weight is not None and (weight.shape != (D,) or weight.dtype != torch.float32):
+        raise ValueError("ssd_gated_rmsnorm_fwd: weight must be float32 [D]")
+    g = D if group_size is None else int(group_size)
+    if out is None:
+        out = torch.empty_like(y)
+    rc = load_library().ssd_gated_rmsnorm_fwd(rows, D, g, _dtype_code(y.dtype), _ptr(y), _ptr(z),
+                                              _ptr(weight), float(eps), _ptr(out),
+                                              _stream_handle(y.device))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_gated_rmsnorm_fwd")
+    return out
 
 
 def ssd_scan_get_status(workspace, device=None) -> int:

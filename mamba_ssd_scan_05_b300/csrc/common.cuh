@@ -75,6 +75,35 @@ struct StepArgs {
 // Recurrent step (step.cu).
 int step_launch(const StepArgs& a);
 
+// Causal depthwise conv1d + SiLU (block.cu), after validation.
+struct ConvArgs {
+    int64_t batch, seqlen, channels;
+    int width;                 // 1..8
+    int32_t dtype;
+    const void* x;             // [batch, seqlen, channels]
+    const float* weight;       // [channels, width]
+    const float* bias;         // [channels] or null
+    const void* s_in;          // [batch, width - 1, channels] or null (zeros)
+    void* s_out;               // [batch, width - 1, channels] or null
+    int silu;
+    void* out;                 // [batch, seqlen, channels]
+    cudaStream_t stream;
+};
+int conv_launch(const ConvArgs& a);
+
+// Gated RMSNorm (block.cu), after validation.
+struct NormArgs {
+    int64_t rows, dim, group_size;
+    int32_t dtype;
+    const void* y;             // [rows, dim]
+    const void* z;             // [rows, dim] or null
+    const float* weight;       // [dim] or null
+    float eps;
+    void* out;                 // [rows, dim]
+    cudaStream_t stream;
+};
+int norm_launch(const NormArgs& a);
+
 // Tensor-core path (tc.cu).
 size_t tc_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t P, int64_t N, int Q);
 bool tc_supports(int32_t dtype, int64_t P, int64_t N, int Q);

@@ -214,6 +214,67 @@ int ssd_step_fwd(const ssd_dims* dims, const void* x, const void* dt, const floa
     return step_launch(a);
 }
 
+int ssd_causal_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t channels, int width,
+                          int32_t dtype, const void* x, const float* weight, const float* bias,
+                          const void* state_in, void* state_out, int silu, void* out,
+                          void* stream) {
+    if (batch < 1 || batch > 65535 || seqlen < 0 || channels < 1 || width < 1 || width > 8)
+        return SSD_ERR_INVALID;
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_INVALID;
+    if ((double)batch * (double)seqlen * (double)channels > 4.0e15) return SSD_ERR_INVALID;
+    if (!weight || (seqlen > 0 && (!x || !out))) return SSD_ERR_INVALID;
+    const size_t eb = elem_bytes(dtype);
+    if (!aligned(x, eb) || !aligned(out, eb) || !aligned(state_in, eb) ||
+        !aligned(state_out, eb) || !aligned(weight, 4) || !aligned(bias, 4))
+        return SSD_ERR_INVALID;
+    if ((seqlen + 31) / 32 > 65535) return SSD_ERR_UNSUPPORTED;
+    // no buffer the kernel writes may overlap one it reads
+    auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
+        if (!a || !b || !na || !nb) return false;
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+        return a0 < b0 + nb && b0 < a0 + na;
+    };
+    const size_t xs = eb * (size_t)(batch * seqlen * channels);
+    const size_t ss = eb * (size_t)(batch * (width - 1) * channels);
+    if (overlap(out, xs, x, xs) || overlap(out, xs, state_in, ss) ||
+        overlap(state_out, ss, x, xs) || overlap(state_out, ss, state_in, ss) ||
+        overlap(state_out, ss, out, xs))
+        return SSD_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (seqlen == 0) {   // nothing to convolve: the state passes through
+        if (!state_out || ss == 0) return SSD_OK;
+        const cudaError_t e = state_in
+                                  ? cudaMemcpyAsync(state_out, state_in, ss,
+                                                    cudaMemcpyDeviceToDevice, st)
+                                  : cudaMemsetAsync(state_out, 0, ss, st);
+        return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    }
+    ConvArgs a;
+    a.batch = batch; a.seqlen = seqlen; a.channels = channels; a.width = width; a.dtype = dtype;
+    a.x = x; a.weight = weight; a.bias = bias; a.s_in = state_in; a.s_out = state_out;
+    a.silu = silu ? 1 : 0; a.out = out; a.stream = st;
+    return conv_launch(a);
+}
+
+int ssd_gated_rmsnorm_fwd(int64_t rows, int64_t dim, int64_t group_size, int32_t dtype,
+                          const void* y, const void* z, const float* weight, float eps,
+                          void* out, void* stream) {
+    if (rows < 0 || dim < 1 || group_size < 1 || dim % group_size != 0) return SSD_ERR_INVALID;
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_INVALID;
+    if (!(eps >= 0.f) || eps > 1.0e30f) return SSD_ERR_INVALID;
+    if (rows > 0 && (!y || !out)) return SSD_ERR_INVALID;
+    const size_t eb = elem_bytes(dtype);
+    if (!aligned(y, eb) || !aligned(z, eb) || !aligned(out, eb) || !aligned(weight, 4))
+        return SSD_ERR_INVALID;
+    if (rows > 0x7fffffffLL || dim / group_size > 12288) return SSD_ERR_UNSUPPORTED;
+    if (rows == 0) return SSD_OK;
+    NormArgs a;
+    a.rows = rows; a.dim = dim; a.group_size = group_size; a.dtype = dtype;
+    a.y = y; a.z = z; a.weight = weight; a.eps = eps; a.out = out;
+    a.stream = static_cast<cudaStream_t>(stream);
+    return norm_launch(a);
+}
+
 int ssd_scan_get_status(void* workspace, void* stream) {
     if (!workspace) return SSD_ERR_INVALID;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -136,3 +136,35 @@ def make_shape_inputs(batch, seqlen, nheads, headdim, dstate, ngroups=1, dtype="
     w = Workload("custom", batch, seqlen, nheads, headdim, dstate, ngroups, 64, dtype,
                  dt_lo=dt_lo, dt_hi=dt_hi, d_mode=d_mode, h0_mode=h0_mode, seed=seed)
     return make_inputs(w)
+
+
+# ---- the block steps around the scan ---------------------------------------------------------
+# Causal conv1d over the scan's input channels of the 2.7B-shaped layer: x, B and C side by side
+# (d_inner + 2 * ngroups * d_state = 5120 + 256 channels), width 4, b = 4, L = 4096.  Weights
+# and bias uniform in +-1/sqrt(width) (the usual Conv1d initialisation), x ~ N(0, 1).
+CONV = {"batch": 4, "seqlen": 4096, "channels": 5376, "width": 4, "dtype": "bf16", "seed": 1200}
+# Gated RMSNorm over the scan's output of the same layer: rows = b * L = 16384 tokens,
+# dim = nheads * headdim = 5120, one group; y, z ~ N(0, 1), weight 1 + N(0, 0.1).
+NORM = {"rows": 16384, "dim": 5120, "group_size": 5120, "dtype": "bf16", "seed": 1300}
+
+
+def make_conv_inputs(batch, seqlen, channels, width, dtype="bf16", seed=0, state=False) -> dict:
+    gen = torch.Generator().manual_seed(seed)
+    T = torch.float32 if dtype == "f32" else torch.bfloat16
+    bound = 1.0 / math.sqrt(width)
+    w = (torch.rand((channels, width), generator=gen) * 2 - 1) * bound
+    bias = (torch.rand(channels, generator=gen) * 2 - 1) * bound
+    x = _randn(gen, (batch, seqlen, channels), 1.0).to(T)
+    st = None
+    if state:
+        st = torch.randn((batch, width - 1, channels), generator=gen).to(T)
+    return dict(x=x, weight=w.contiguous(), bias=bias.contiguous(), state=st)
+
+
+def make_norm_inputs(rows, dim, dtype="bf16", seed=0) -> dict:
+    gen = torch.Generator().manual_seed(seed)
+    T = torch.float32 if dtype == "f32" else torch.bfloat16
+    y = torch.randn((rows, dim), generator=gen).to(T)
+    z = torch.randn((rows, dim), generator=gen).to(T)
+    w = 1.0 + math.sqrt(0.1) * torch.randn(dim, generator=gen)
+    return dict(y=y, z=z, weight=w.contiguous())
