@@ -205,6 +205,23 @@ def dist_setup():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device, world: int) -> float:
+    """The largest `value` over all ranks (one float; the timing of the slowest rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Replicas: every rank processes the same number of units, so the job processes
+    world * units_per_rank units in the slowest rank's time."""
+    return units_per_rank * world / seconds
+
+
 def workload_config(w, extra: dict) -> dict:
     cfg = {"workload": w.describe(), "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
            "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk}
@@ -600,13 +617,10 @@ def main():
     status = m.ssd_scan_get_status(workspace)
     total_ms = ev0.elapsed_time(ev1)
     call_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev, ws)
     ms_per_step = total_ms / args.steps
     tokens_all = w.tokens * ws
-    value = tokens_all / (total_ms / 1e3 / args.steps) / 1.0
+    value = whole_job_rate(w.tokens, ws, ms_per_step / 1e3)
 
     # end to end through the host-buffer entry point (pinned host memory, copies timed)
     e2e = None
@@ -628,10 +642,7 @@ def main():
             m.ssd_scan_fwd_host(*args_h, chunk_size=w.chunk, y=y_h, final_state=h_h,
                                 arena=arena, device=dev)
         t_e2e = time.perf_counter() - t0
-        if ws > 1:
-            t = torch.tensor([t_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = float(t.item())
+        t_e2e = max_over_ranks(t_e2e, dev, ws)
         h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
         d2h = y_h.numel() * y_h.element_size() + h_h.numel() * h_h.element_size()
         e2e = {"value": tokens_all * args.e2e_steps / t_e2e, "unit": "tokens/s",
