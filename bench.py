@@ -504,6 +504,95 @@ def run_block(args, op, local):
     return 0
 
 
+def run_varlen(args, local):
+    """The scan over a packed batch of variable-length sequences (ssd_scan_fwd_varlen)."""
+    import torch
+    import mamba_ssd_scan_05_b300 as m
+    from mamba_ssd_scan_05_b300 import workloads
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    v = workloads.VARLEN
+    lengths = workloads.varlen_lengths(v["nseq"], v["min_len"], v["max_len"], v["seed"])
+    inp = workloads.make_varlen_inputs(lengths, v["nheads"], v["headdim"], v["dstate"],
+                                       v["ngroups"], v["dtype"], seed=v["seed"])
+    d = {k: (x.to(dev) if torch.is_tensor(x) else x) for k, x in inp.items()}
+    cu = inp["cu_seqlens"]
+    total = cu[-1]
+    nseq = len(lengths)
+    y = torch.empty_like(d["x"])
+    hT = torch.empty_like(d["h0"])
+    dims = m.make_dims(d["x"], d["B"])
+    ws_t = torch.empty(m.ssd_scan_varlen_workspace_bytes(dims, cu, v["chunk"]), dtype=torch.uint8,
+                       device=dev)
+
+    def call():
+        m.ssd_scan_fwd_varlen(d["x"], d["dt"], d["A"], d["B"], d["C"], cu, d["D"], d["h0"],
+                              chunk_size=v["chunk"], y=y, final_states=hT, workspace=ws_t)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    if m.ssd_scan_get_status(ws_t) != 0:
+        raise SystemExit("device status error during warm-up")
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        graph.replay()
+        ends[i].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    status = m.ssd_scan_get_status(ws_t)
+    total_ms = ev0.elapsed_time(ev1)
+    call_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms_per_step = total_ms / args.steps
+    # algorithmic bytes: x, dt, B, C, y once, A and D, the initial and final states
+    eb = d["x"].element_size()
+    H, P, N, G = v["nheads"], v["headdim"], v["dstate"], v["ngroups"]
+    nbytes = (eb * total * (2 * H * P + H + 2 * G * N) + 8 * H + 2 * 4 * nseq * H * P * N)
+    peaks, peak_src = load_peaks()
+    avg_call_s = statistics.mean(call_ms) / 1e3
+    achieved = nbytes / avg_call_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
+                "t_roof_us": 1e6 * nbytes / (peaks["hbm_gbs"] * 1e9), "algorithmic_bytes": nbytes,
+                "kernel": "ssd_tc_kernel", "timed": "one ssd_scan_fwd_varlen call (CUDA graph replay)"}
+    line = {
+        "metric": "SSD scan fwd over a packed variable-length batch, tokens/s on 1 B300; % of roofline (HBM)",
+        "value": total / (ms_per_step / 1e3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": v["dtype"],
+        "data": "synthetic",
+        "config": dict(v, workload=f"varlen-2.7b: {nseq} sequences, {total} tokens, lengths "
+                                   f"{min(lengths)}..{max(lengths)}, H={H} P={P} N={N} bf16",
+                       lengths=lengths, op="varlen", parallelism="replicas x1",
+                       l2=f"{nbytes / 1e6:.0f} MB moved per call (larger than L2)"),
+        "roofline": roofline, "cpu_baseline": None, "e2e": None,
+        "gpu_launches": args.steps * sum(1 for n in lengths if n > 0),
+        "clocks": sampler.summary(wall0, wall1), "device_status": status,
+        "per_call_ms": {"median": statistics.median(call_ms), "min": min(call_ms),
+                        "max": max(call_ms)},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -515,7 +604,7 @@ def main():
     ap.add_argument("--path", type=int, default=-1, help="kernel family (-1 auto, 0 chunked, 1 tc)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["scan", "step", "conv", "norm"], default="scan",
+    ap.add_argument("--op", choices=["scan", "step", "conv", "norm", "varlen"], default="scan",
                     help="scan: the forward scan (default); step: the recurrent decode step; "
                          "conv / norm: the block steps before / after the scan")
     args = ap.parse_args()
@@ -527,6 +616,8 @@ def main():
             raise SystemExit(f"--op {args.op}: our arm on one GPU only")
         if args.op == "step":
             return run_step(args, ws, rank, local)
+        if args.op == "varlen":
+            return run_varlen(args, local)
         return run_block(args, args.op, local)
 
     from mamba_ssd_scan_05_b300 import workloads

@@ -31,8 +31,8 @@
  *       y              [batch, seqlen, nheads, headdim]   T   (written)
  *       final_state    [batch, nheads, headdim, dstate]   float32 (written), or NULL
  *     Head h reads B/C group h / (nheads / ngroups).
- *   - Base pointers of x, dt, B, C, y must be 16-byte aligned; initial_state and final_state
- *     4-byte aligned; workspace 256-byte aligned.
+ *   - Base pointers of x, B, C, y must be 16-byte aligned; dt aligned to its element size;
+ *     initial_state and final_state 4-byte aligned; workspace 256-byte aligned.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every
  *     launch and copy is enqueued on it; the functions return without synchronising, except
  *     ssd_scan_get_status, which synchronises `stream`.
@@ -165,6 +165,37 @@ int ssd_scan_fwd_noalloc(const ssd_dims* dims,
                          void* y, float* final_state, void* stream);
 
 /*
+ * ssd_scan_fwd_varlen -- the scan over a packed batch of variable-length sequences: batch row
+ * 0 of `dims` holds nseq sequences back to back, sequence i being tokens cu_seqlens[i] ..
+ * cu_seqlens[i+1] - 1.  Each sequence starts from its own initial state (the state resets at
+ * every sequence start: youngju.dev article, section "状態初期化とシーケンス境界") and
+ * ends in its own final state; y is written for every token.
+ *
+ *   - dims.batch == 1, dims.seqlen = total tokens; cu_seqlens is a HOST array of nseq + 1
+ *     non-decreasing offsets with cu_seqlens[0] = 0 and cu_seqlens[nseq] = dims.seqlen.
+ *     Empty sequences are allowed (final state = initial state).
+ *   - x, dt, B, C, y as for ssd_scan_fwd with batch 1; initial_state / final_state are
+ *     [nseq, nheads, headdim, dstate] float32 (each nullable as for ssd_scan_fwd).
+ *   - nheads * headdim and ngroups * dstate elements must each be a multiple of 16 bytes, so
+ *     that every sequence's x, y, B and C slices start on a 16-byte boundary
+ *     (else SSD_ERR_UNSUPPORTED).
+ *   - workspace: at least ssd_scan_varlen_workspace_bytes (the largest single sequence's
+ *     need).  `path` as for ssd_scan_fwd_path, or SSD_PATH_AUTO.
+ *   - Enqueues one scan per non-empty sequence on `stream`, in order, sharing the workspace.
+ *     The status word is cleared once, so ssd_scan_get_status reports a device-side failure in
+ *     any of them.  Returns as ssd_scan_fwd; every sequence is checked before anything is
+ *     enqueued.
+ */
+size_t ssd_scan_varlen_workspace_bytes(const ssd_dims* dims, const int64_t* cu_seqlens,
+                                       int64_t nseq, int chunk_size, int path);
+int ssd_scan_fwd_varlen(const ssd_dims* dims, const int64_t* cu_seqlens, int64_t nseq,
+                        const void* x, const void* dt, const float* A,
+                        const void* B, const void* C, const float* D,
+                        const float* initial_state, int chunk_size,
+                        void* y, float* final_state,
+                        void* workspace, size_t workspace_bytes, void* stream, int path);
+
+/*
  * ssd_step_fwd -- one recurrent step per (batch row, head): the scan above for a single token,
  * for decoding, where tokens arrive one at a time and the state lives between calls.
  *
@@ -181,8 +212,8 @@ int ssd_scan_fwd_noalloc(const ssd_dims* dims,
  *   - state_in, state_out: [batch, nheads, headdim, dstate] float32, device memory.  state_in
  *     NULL means a zero state; state_out is required and is written completely.  state_out may
  *     equal state_in (update in place); otherwise the two must not overlap.
- *   - D may be NULL (no skip term).  Alignment as for ssd_scan_fwd (x, dt, B, C, y 16 bytes;
- *     A, D and the states 4 bytes).
+ *   - D may be NULL (no skip term).  Alignment as for ssd_scan_fwd (x, B, C, y 16 bytes; dt
+ *     its element size; A, D and the states 4 bytes).
  *   - Needs no workspace and allocates nothing.  Enqueued on `stream`.
  *   - Returns SSD_OK once enqueued; SSD_ERR_INVALID for bad arguments (including seqlen != 1 or
  *     partially overlapping states), SSD_ERR_UNSUPPORTED if batch * nheads exceeds 2^31 - 1,

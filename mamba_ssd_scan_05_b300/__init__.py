@@ -23,10 +23,12 @@ from ._binding import (  # noqa: F401
     ssd_dims,
     ssd_scan_fwd,
     ssd_scan_fwd_host,
+    ssd_scan_fwd_varlen,
     ssd_scan_get_status,
     ssd_scan_host_arena_bytes,
     ssd_scan_resolve_path,
     ssd_scan_strerror,
+    ssd_scan_varlen_workspace_bytes,
     ssd_scan_version,
     ssd_scan_workspace_bytes,
     ssd_step_fwd,

@@ -72,6 +72,12 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_gated_rmsnorm_fwd.argtypes = [i64, i64, i64, i32, vp, vp, fp, ctypes.c_float,
                                               vp, vp]
         lib.ssd_gated_rmsnorm_fwd.restype = i32
+        cu_p = ctypes.POINTER(ctypes.c_int64)
+        lib.ssd_scan_varlen_workspace_bytes.argtypes = [dims_p, cu_p, i64, i32, i32]
+        lib.ssd_scan_varlen_workspace_bytes.restype = sz
+        lib.ssd_scan_fwd_varlen.argtypes = [dims_p, cu_p, i64, vp, vp, fp, vp, vp, fp, fp, i32,
+                                            vp, fp, vp, sz, vp, i32]
+        lib.ssd_scan_fwd_varlen.restype = i32
         lib.ssd_scan_get_status.argtypes = [vp, vp]
         lib.ssd_scan_get_status.restype = i32
         lib.ssd_scan_strerror.argtypes = [i32]
@@ -177,6 +183,58 @@ def ssd_scan_fwd(x, dt, A, B, C, D=None, initial_state=None, chunk_size: int = 2
     if rc != SSD_OK:
         raise SSDError(rc, "ssd_scan_fwd")
     return y, final_state
+
+
+def _cu_array(cu_seqlens):
+    vals = [int(v) for v in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+    return (ctypes.c_int64 * len(vals))(*vals), len(vals) - 1
+
+
+def ssd_scan_varlen_workspace_bytes(dims: ssd_dims, cu_seqlens, chunk_size: int,
+                                    path: int = SSD_PATH_AUTO) -> int:
+    cu, nseq = _cu_array(cu_seqlens)
+    return load_library().ssd_scan_varlen_workspace_bytes(ctypes.byref(dims), cu, nseq,
+                                                          int(chunk_size), int(path))
+
+
+def ssd_scan_fwd_varlen(x, dt, A, B, C, cu_seqlens, D=None, initial_states=None,
+                        chunk_size: int = 256, path: int = SSD_PATH_AUTO, y=None,
+                        final_states=None, workspace=None, return_final_states: bool = True):
+    """The scan over a packed batch: x [1, total, H, P] (and dt, B, C alike) holds the
+    sequences back to back, sequence i being tokens cu_seqlens[i] .. cu_seqlens[i+1] - 1 (a
+    host list or CPU tensor).  Each sequence starts from initial_states[i] (or zeros).
+    Returns (y, final_states [nseq, H, P, N])."""
+    if x.dim() != 4 or x.shape[0] != 1:
+        raise ValueError("ssd_scan_fwd_varlen: x must be [1, total, H, P]")
+    _check_inputs(x, dt, A, B, C, D, None)
+    if not x.is_cuda:
+        raise ValueError("ssd_scan_fwd_varlen: tensors must be on a CUDA device")
+    cu, nseq = _cu_array(cu_seqlens)
+    _, L, H, P = x.shape
+    N = B.shape[3]
+    if initial_states is not None and (initial_states.shape != (nseq, H, P, N)
+                                       or initial_states.dtype != torch.float32
+                                       or not initial_states.is_contiguous()):
+        raise ValueError("ssd_scan_fwd_varlen: initial_states must be float32 [nseq,H,P,N]")
+    lib = load_library()
+    dims = make_dims(x, B)
+    if y is None:
+        y = torch.empty_like(x)
+    if final_states is None and return_final_states:
+        final_states = torch.empty((nseq, H, P, N), dtype=torch.float32, device=x.device)
+    need = lib.ssd_scan_varlen_workspace_bytes(ctypes.byref(dims), cu, nseq, int(chunk_size),
+                                               int(path))
+    if need == 0:
+        raise SSDError(SSD_ERR_INVALID, "ssd_scan_varlen_workspace_bytes")
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    rc = lib.ssd_scan_fwd_varlen(ctypes.byref(dims), cu, nseq, _ptr(x), _ptr(dt), _ptr(A),
+                                 _ptr(B), _ptr(C), _ptr(D), _ptr(initial_states),
+                                 int(chunk_size), _ptr(y), _ptr(final_states), _ptr(workspace),
+                                 workspace.numel(), _stream_handle(x.device), int(path))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_scan_fwd_varlen")
+    return y, final_states
 
 
 def ssd_step_fwd(x, dt, A, B, C, D=None, state=None, state_out=None, y=None):

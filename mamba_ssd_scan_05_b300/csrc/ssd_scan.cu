@@ -2,6 +2,8 @@
 // host-buffer variant and status reporting.  Every declaration is in include/ssd_scan.h.
 #include <string.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 using namespace ssd;
@@ -58,19 +60,22 @@ size_t workspace_for(const ssd_dims* d, int chunk_size, int resolved) {
 
 int run(const ssd_dims* d, const void* x, const void* dt, const float* A, const void* B,
         const void* C, const float* D, const float* h0, int chunk_size, void* y, float* hT,
-        void* workspace, size_t workspace_bytes, void* stream, int path) {
+        void* workspace, size_t workspace_bytes, void* stream, int path,
+        bool clear_status = true) {
     const int r = resolve(d, chunk_size, path);
     if (r < 0) return -r;
     if (!A || (d->seqlen > 0 && (!x || !dt || !B || !C || !y))) return SSD_ERR_INVALID;
-    if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(B, 16) || !aligned(C, 16) ||
-        !aligned(y, 16) || !aligned(A, 4) || !aligned(D, 4) || !aligned(h0, 4) ||
-        !aligned(hT, 4))
+    // x, B, C and y are moved in 16-byte vectors (and by TMA); dt is read element-wise
+    if (!aligned(x, 16) || !aligned(dt, elem_bytes(d->dtype)) || !aligned(B, 16) ||
+        !aligned(C, 16) || !aligned(y, 16) || !aligned(A, 4) || !aligned(D, 4) ||
+        !aligned(h0, 4) || !aligned(hT, 4))
         return SSD_ERR_INVALID;
     if (!workspace || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
     if (workspace_bytes < workspace_for(d, chunk_size, r)) return SSD_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the status word reports on this call only
-    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
+    if (clear_status && cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess)
+        return SSD_ERR_CUDA;
     if (d->seqlen == 0) {
         if (!hT) return SSD_OK;
         const size_t sb = sizeof(float) * (size_t)(d->batch * d->nheads * d->headdim * d->dstate);
@@ -185,6 +190,86 @@ int ssd_scan_fwd_host(const ssd_dims* dims, const void* x, const void* dt, const
     return SSD_OK;
 }
 
+// Sequence i of a packed batch as a one-row problem: tokens cu[i] .. cu[i+1] - 1.
+static bool varlen_dims(const ssd_dims* dims, const int64_t* cu, int64_t i, ssd_dims* out) {
+    *out = *dims;
+    out->batch = 1;
+    out->seqlen = cu[i + 1] - cu[i];
+    return true;
+}
+
+static int check_varlen(const ssd_dims* dims, const int64_t* cu, int64_t nseq) {
+    if (!dims || !cu || nseq < 1 || dims->batch != 1) return SSD_ERR_INVALID;
+    if (cu[0] != 0 || cu[nseq] != dims->seqlen) return SSD_ERR_INVALID;
+    for (int64_t i = 0; i < nseq; ++i)
+        if (cu[i + 1] < cu[i]) return SSD_ERR_INVALID;
+    return SSD_OK;
+}
+
+size_t ssd_scan_varlen_workspace_bytes(const ssd_dims* dims, const int64_t* cu_seqlens,
+                                       int64_t nseq, int chunk_size, int path) {
+    if (check_varlen(dims, cu_seqlens, nseq) != SSD_OK) return 0;
+    size_t need = 0;
+    for (int64_t i = 0; i < nseq; ++i) {
+        ssd_dims di;
+        varlen_dims(dims, cu_seqlens, i, &di);
+        if (di.seqlen == 0) continue;
+        const int r = resolve(&di, chunk_size, path);
+        if (r < 0) return 0;
+        need = std::max(need, workspace_for(&di, chunk_size, r));
+    }
+    return std::max(need, (size_t)kWsHeaderBytes);
+}
+
+int ssd_scan_fwd_varlen(const ssd_dims* dims, const int64_t* cu_seqlens, int64_t nseq,
+                        const void* x, const void* dt, const float* A, const void* B,
+                        const void* C, const float* D, const float* initial_state,
+                        int chunk_size, void* y, float* final_state, void* workspace,
+                        size_t workspace_bytes, void* stream, int path) {
+    int rc = check_varlen(dims, cu_seqlens, nseq);
+    if (rc != SSD_OK) return rc;
+    rc = check_dims(dims, chunk_size);
+    if (rc != SSD_OK) return rc;
+    // every sequence must resolve and fit the workspace before anything is enqueued
+    const size_t need = ssd_scan_varlen_workspace_bytes(dims, cu_seqlens, nseq, chunk_size, path);
+    if (need == 0) return SSD_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
+    if (workspace_bytes < need) return SSD_ERR_WORKSPACE;
+    const size_t eb = elem_bytes(dims->dtype);
+    const int64_t H = dims->nheads, P = dims->headdim, N = dims->dstate, G = dims->ngroups;
+    // the x, y, B and C slices of every sequence start on 16-byte boundaries
+    if ((H * P * eb) % 16 || (G * N * eb) % 16) return SSD_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
+    const size_t state_elems = (size_t)(H * P * N);
+    for (int64_t i = 0; i < nseq; ++i) {
+        ssd_dims di;
+        varlen_dims(dims, cu_seqlens, i, &di);
+        const int64_t t0 = cu_seqlens[i];
+        const uint8_t* xb = static_cast<const uint8_t*>(x);
+        const uint8_t* dtb = static_cast<const uint8_t*>(dt);
+        const uint8_t* Bb = static_cast<const uint8_t*>(B);
+        const uint8_t* Cb = static_cast<const uint8_t*>(C);
+        uint8_t* yb = static_cast<uint8_t*>(y);
+        const float* h0 = initial_state ? initial_state + i * state_elems : nullptr;
+        float* hT = final_state ? final_state + i * state_elems : nullptr;
+        if (di.seqlen == 0) {   // an empty sequence: its final state is its initial state
+            if (!hT) continue;
+            const size_t sb = sizeof(float) * state_elems;
+            const cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, sb, cudaMemcpyDeviceToDevice, st)
+                                     : cudaMemsetAsync(hT, 0, sb, st);
+            if (e != cudaSuccess) return SSD_ERR_CUDA;
+            continue;
+        }
+        rc = run(&di, xb + eb * (size_t)(t0 * H * P), dtb + eb * (size_t)(t0 * H), A,
+                 Bb + eb * (size_t)(t0 * G * N), Cb + eb * (size_t)(t0 * G * N), D, h0,
+                 chunk_size, yb + eb * (size_t)(t0 * H * P), hT, workspace, workspace_bytes,
+                 stream, path, /*clear_status=*/false);
+        if (rc != SSD_OK) return rc;
+    }
+    return SSD_OK;
+}
+
 int ssd_step_fwd(const ssd_dims* dims, const void* x, const void* dt, const float* A,
                  const void* B, const void* C, const float* D, const float* state_in,
                  float* state_out, void* y, void* stream) {
@@ -192,9 +277,9 @@ int ssd_step_fwd(const ssd_dims* dims, const void* x, const void* dt, const floa
     const int rc = check_dims(dims, 1);
     if (rc != SSD_OK) return rc;
     if (!x || !dt || !A || !B || !C || !y || !state_out) return SSD_ERR_INVALID;
-    if (!aligned(x, 16) || !aligned(dt, 16) || !aligned(B, 16) || !aligned(C, 16) ||
-        !aligned(y, 16) || !aligned(A, 4) || !aligned(D, 4) || !aligned(state_in, 4) ||
-        !aligned(state_out, 4))
+    if (!aligned(x, 16) || !aligned(dt, elem_bytes(dims->dtype)) || !aligned(B, 16) ||
+        !aligned(C, 16) || !aligned(y, 16) || !aligned(A, 4) || !aligned(D, 4) ||
+        !aligned(state_in, 4) || !aligned(state_out, 4))
         return SSD_ERR_INVALID;
     // the state is updated in place or copied to a separate buffer, never a partial overlap
     const size_t sb = sizeof(float) * (size_t)(dims->batch * dims->nheads * dims->headdim *

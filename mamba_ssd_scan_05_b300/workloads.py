@@ -168,3 +168,33 @@ def make_norm_inputs(rows, dim, dtype="bf16", seed=0) -> dict:
     z = torch.randn((rows, dim), generator=gen).to(T)
     w = 1.0 + math.sqrt(0.1) * torch.randn(dim, generator=gen)
     return dict(y=y, z=z, weight=w.contiguous())
+
+
+# Packed variable-length batch on the 2.7B-shaped layer's heads: 24 sequences whose lengths are
+# log-uniform in [64, 4096] (one draw from the seed), back to back in one row, each with its
+# own initial state N(0, 0.1).
+VARLEN = {"nseq": 24, "min_len": 64, "max_len": 4096, "nheads": 80, "headdim": 64,
+          "dstate": 128, "ngroups": 1, "chunk": 256, "dtype": "bf16", "seed": 1400}
+
+
+def varlen_lengths(nseq, min_len, max_len, seed) -> list:
+    gen = torch.Generator().manual_seed(seed)
+    u = torch.rand(nseq, generator=gen, dtype=torch.float64)
+    lo, hi = math.log(min_len), math.log(max_len)
+    return [int(round(math.exp(lo + float(v) * (hi - lo)))) for v in u]
+
+
+def make_varlen_inputs(lengths, nheads, headdim, dstate, ngroups=1, dtype="bf16", seed=0) -> dict:
+    """One packed row of the given sequence lengths (inputs drawn like the scan workloads) plus
+    cu_seqlens and per-sequence initial states."""
+    total = int(sum(lengths))
+    inp = make_shape_inputs(1, total, nheads, headdim, dstate, ngroups, dtype, seed=seed,
+                            d_mode="normal")
+    gen = torch.Generator().manual_seed(seed + 1)
+    inp["h0"] = math.sqrt(0.1) * torch.randn((len(lengths), nheads, headdim, dstate),
+                                             generator=gen, dtype=torch.float32)
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+    inp["cu_seqlens"] = cu
+    return inp

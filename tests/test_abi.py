@@ -135,3 +135,13 @@ def test_step_argument_checks_need_no_gpu(lib):
     # states overlapping without being the same buffer
     assert call(dims(L=1, b=1, H=1, P=4, N=4), s_in=ctypes.c_void_p(1 << 20),
                 s_out=ctypes.c_void_p((1 << 20) + 16)) == 1
+
+
+def test_varlen_workspace_checks_offsets(lib):
+    import mamba_ssd_scan_05_b300 as m
+    d = dims(b=1, L=300, H=8, P=64, N=128)
+    good = m.ssd_scan_varlen_workspace_bytes(d, [0, 100, 100, 300], 128)
+    assert good >= m.ssd_scan_workspace_bytes(dims(b=1, L=200, H=8, P=64, N=128), 128)
+    assert m.ssd_scan_varlen_workspace_bytes(d, [0, 100, 299], 128) == 0      # wrong total
+    assert m.ssd_scan_varlen_workspace_bytes(d, [0, 200, 100, 300], 128) == 0  # decreasing
+    assert m.ssd_scan_varlen_workspace_bytes(dims(b=2, L=300), [0, 300], 128) == 0  # batch != 1
