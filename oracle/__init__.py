@@ -23,9 +23,10 @@ Three independent float64 forms of the same method, each written from the pages:
                the attention-like dual form with the decay mask exp(cum_i - cum_j); between
                chunks the state recurrence (Qiita article section 4.2, "chunk内は行列積、chunk間は
                スキャン"; youngju.dev article, section "SSDアルゴリズムとチャンク分割", the
-               ``_chunk_scan`` listing).  Readings where that listing is incomplete (it omits dt_j
-               on the key side, has no inter-chunk pass and exponentiates before masking) are
-               listed in the design doc.  Exposes the per-stage intermediates.
+               ``_chunk_scan`` listing).  That listing is incomplete: it omits dt_j on the key
+               side, has no inter-chunk pass and exponentiates before masking.  This form
+               multiplies by dt_j (Bbar = dt B), adds the state pass between chunks and masks
+               before the exponential.  Exposes the per-stage intermediates.
 
 Layouts (row-major, any float dtype in, float64 out):
     x  [b, L, H, P]   dt [b, L, H]   A [H]   B, C [b, L, G, N]   D [H]   h0 [b, H, P, N]

@@ -20,9 +20,9 @@ TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-b
                    features:
                        out[r, i] = y[r, i] / sqrt(mean_{j in group(i)} y[r, j]^2 + eps)
                                    * w[i] * silu(z[r, i]).
-                   The pages fix neither eps nor the weight; the readings (eps a parameter,
-                   default 1e-5; weight a per-feature vector, ones when absent; z absent means
-                   no gate) are listed in the design doc.
+                   The pages fix neither eps nor the weight: eps is a parameter (default
+                   1e-5), the weight a per-feature vector (ones when absent), and an absent z
+                   means no gate.
 
 silu(v) = v / (1 + exp(-v)).  Inputs of any float dtype (numpy or torch) are upcast to float64.
 """
