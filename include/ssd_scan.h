@@ -241,7 +241,8 @@ int ssd_step_fwd(const ssd_dims* dims,
  *   - state_in:     [batch, width - 1, channels] T, or NULL: the width - 1 inputs before x
  *   - state_out:    [batch, width - 1, channels] T, or NULL (not written): the last width - 1
  *                   inputs of state_in ++ x, so the next call continues the sequence
- *   - 1 <= width <= 8, batch <= 65535, seqlen <= 2^21 - 32.  Element alignment suffices;
+ *   - 1 <= width <= 8, batch <= 65535, seqlen <= 1048560 (65535 blocks of 16 tokens; longer
+ *     sequences: SSD_ERR_UNSUPPORTED, or split them and carry the state).  Element alignment suffices;
  *     16-byte aligned buffers with channels % (16 / sizeof(T)) == 0 take the vector path.
  *   - No output may overlap an input, and state_out may not overlap out (SSD_ERR_INVALID).
  *   - Needs no workspace; enqueued on `stream`.  Returns SSD_OK, SSD_ERR_INVALID,

@@ -209,6 +209,8 @@ int conv_launch_k(int K, dim3 grid, cudaStream_t st, const ConvParams& p) {
 
 template <typename T, int VEC>
 int conv_launch_t(const ConvArgs& a, const ConvParams& p) {
+    // grid y counts token blocks (at most 65535), grid z batch rows (checked by the caller)
+    if ((a.seqlen + kConvTokens - 1) / kConvTokens > 65535) return SSD_ERR_UNSUPPORTED;
     const int64_t threads_c = (a.channels + VEC - 1) / VEC;
     const dim3 grid((unsigned)((threads_c + kConvThreads - 1) / kConvThreads),
                     (unsigned)((a.seqlen + kConvTokens - 1) / kConvTokens), (unsigned)a.batch);

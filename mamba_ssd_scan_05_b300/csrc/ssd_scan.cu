@@ -312,7 +312,6 @@ int ssd_causal_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t channels, int w
     if (!aligned(x, eb) || !aligned(out, eb) || !aligned(state_in, eb) ||
         !aligned(state_out, eb) || !aligned(weight, 4) || !aligned(bias, 4))
         return SSD_ERR_INVALID;
-    if ((seqlen + 31) / 32 > 65535) return SSD_ERR_UNSUPPORTED;
     // no buffer the kernel writes may overlap one it reads
     auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
         if (!a || !b || !na || !nb) return false;
