@@ -68,7 +68,7 @@ def load_peaks():
 
 # Source files each profiled kernel is built from (a traffic record is valid for these bytes).
 KERNEL_SOURCES = {
-    "ssd_tc_kernel": ("tc.cu", "tc_ptx.cuh", "common.cuh"),
+    "ssd_tc_kernel": ("tc.cu", "tc_plan.cuh", "tc_ptx.cuh", "common.cuh"),
     "step_kernel_vec": ("step.cu", "common.cuh"),
     "conv_kernel": ("block.cu", "common.cuh"),
     "norm_kernel": ("block.cu", "common.cuh"),

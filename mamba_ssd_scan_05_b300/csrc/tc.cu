@@ -46,12 +46,14 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "tc_plan.cuh"
 #include "tc_ptx.cuh"
 
 namespace ssd {
 namespace {
 
 using namespace ptx;
+using namespace plan;
 
 constexpr int kTile = 128;          // tokens per tile (MMA M)
 constexpr int kPS = 64;             // headdim columns per unit (MMA N of Y, Y_off, S)
@@ -118,31 +120,6 @@ struct Cfg {
     static_assert(kXSt <= kXStagesMax, "x ring");
 };
 
-enum : int { kInitH0 = 0, kInitZero = 1, kInitLookback = 2 };
-enum : int { kFinNone = 0, kFinFinal = 1, kFinIncl = 2, kFinAgg = 3 };
-
-// Unit indices and coordinates fit in 32 bits (the launcher checks batch * H * P/64).
-struct Item {
-    int u;            // unit
-    int k0, k1;       // tile range of the unit's chain
-    int pass1;        // 1: state-only pass (no y)
-    int init;         // how the state starts: kInit*
-    int fin;          // what happens to the state at the end: kFin*
-};
-
-// A CTA's range, as scalars (no arrays, so nothing of it lives in local memory).
-//
-// A range holds at most a tail piece of one chain (it needs the state the previous range
-// ends with), whole chains, and a head piece of another chain (its end state is needed by the
-// next range); or a middle piece of one chain.  Items run in this order: [state-only pass over
-// the piece with a successor, in pass1 mode], [head piece], [whole chains], [tail piece], so
-// the state a successor needs is published as early as possible and the state a range needs
-// is consumed as late as possible.
-struct Plan {
-    int u0, u1, f_lo, n_full, n_items;
-    int k0, k1, n_pre, middle, p1;
-};
-
 struct TcParams {
     int64_t batch, L, H, P, N, G;
     int n_ps;           // P / 64
@@ -177,50 +154,7 @@ struct Small {
 };
 
 __device__ __forceinline__ Plan make_plan(const TcParams& p, int cta) {
-    Plan pl;
-    pl.u0 = pl.u1 = pl.f_lo = pl.n_full = pl.n_items = 0;
-    pl.k0 = pl.k1 = pl.n_pre = pl.middle = 0;
-    pl.p1 = p.pass1_mode != 0;
-    const int64_t T = p.n_tiles, total = p.n_units * T;
-    const int64_t start = (int64_t)cta * total / p.n_ctas;
-    const int64_t end = (int64_t)(cta + 1) * total / p.n_ctas;
-    if (start >= end) return pl;
-    pl.u0 = (int)(start / T);
-    pl.u1 = (int)((end - 1) / T);
-    pl.k0 = (int)(start % T);
-    pl.k1 = (int)((end - 1) % T + 1);
-    if (pl.u0 == pl.u1 && pl.k0 > 0 && pl.k1 < T) {     // middle piece of one chain
-        pl.middle = 1;
-        pl.n_pre = pl.p1;
-        pl.n_items = pl.n_pre + 1;
-        return pl;
-    }
-    // head piece of chain u1 (starts at tile 0, ends before T); tail piece of chain u0
-    const bool head = (pl.u0 == pl.u1) ? (pl.k0 == 0 && pl.k1 < T) : (pl.k1 < T);
-    const bool tail = pl.k0 > 0;
-    pl.n_pre = head ? 1 + pl.p1 : 0;
-    const int f_first = tail ? pl.u0 + 1 : pl.u0;
-    const int f_last = head ? pl.u1 - 1 : pl.u1;
-    if (f_last >= f_first) {
-        pl.f_lo = f_first;
-        pl.n_full = f_last - f_first + 1;
-    }
-    pl.n_items = pl.n_pre + pl.n_full + (tail ? 1 : 0);
-    return pl;
-}
-
-__device__ __forceinline__ Item plan_item(const Plan& pl, int i, int T) {
-    if (pl.middle) {
-        if (pl.n_pre > 0 && i == 0) return Item{pl.u0, pl.k0, pl.k1, 1, kInitZero, kFinAgg};
-        return Item{pl.u0, pl.k0, pl.k1, 0, kInitLookback, kFinIncl};
-    }
-    if (i < pl.n_pre) {
-        if (pl.p1 && i == 0) return Item{pl.u1, 0, pl.k1, 1, kInitH0, kFinIncl};
-        return Item{pl.u1, 0, pl.k1, 0, kInitH0, pl.p1 ? kFinNone : kFinIncl};
-    }
-    i -= pl.n_pre;
-    if (i < pl.n_full) return Item{pl.f_lo + i, 0, T, 0, kInitH0, kFinFinal};
-    return Item{pl.u0, pl.k0, (pl.u0 == pl.u1) ? pl.k1 : T, 0, kInitLookback, kFinFinal};
+    return plan::make_plan(p.n_units, p.n_tiles, p.n_ctas, p.pass1_mode, cta);
 }
 
 struct UnitCoords {

@@ -1,0 +1,91 @@
+// tc_plan.cuh -- the work plan of the tensor-core scan kernel: how the tile chains of all
+// units are cut into one contiguous range per CTA, and the items (chain pieces) each CTA runs.
+// Plain integer arithmetic, compiled for the device (the kernel) and for the host (the plan
+// checks in the tests).  Internal to libssd_scan.
+#pragma once
+
+#include <stdint.h>
+
+#ifdef __CUDACC__
+#define SSD_HD __host__ __device__ __forceinline__
+#else
+#define SSD_HD inline
+#endif
+
+namespace ssd {
+namespace plan {
+
+enum : int { kInitH0 = 0, kInitZero = 1, kInitLookback = 2 };
+enum : int { kFinNone = 0, kFinFinal = 1, kFinIncl = 2, kFinAgg = 3 };
+
+// Unit indices and coordinates fit in 32 bits (the launcher checks batch * H * P/64).
+struct Item {
+    int u;            // unit
+    int k0, k1;       // tile range of the unit's chain
+    int pass1;        // 1: state-only pass (no y)
+    int init;         // how the state starts: kInit*
+    int fin;          // what happens to the state at the end: kFin*
+};
+
+// A CTA's range, as scalars (no arrays, so nothing of it lives in local memory).
+//
+// A range holds at most a tail piece of one chain (it needs the state the previous range
+// ends with), whole chains, and a head piece of another chain (its end state is needed by the
+// next range); or a middle piece of one chain.  Items run in this order: [state-only pass over
+// the piece with a successor, in pass1 mode], [head piece], [whole chains], [tail piece], so
+// the state a successor needs is published as early as possible and the state a range needs
+// is consumed as late as possible.
+struct Plan {
+    int u0, u1, f_lo, n_full, n_items;
+    int k0, k1, n_pre, middle, p1;
+};
+
+SSD_HD Plan make_plan(int64_t n_units, int n_tiles, int n_ctas, int pass1_mode, int cta) {
+    Plan pl;
+    pl.u0 = pl.u1 = pl.f_lo = pl.n_full = pl.n_items = 0;
+    pl.k0 = pl.k1 = pl.n_pre = pl.middle = 0;
+    pl.p1 = pass1_mode != 0;
+    const int64_t T = n_tiles, total = n_units * T;
+    const int64_t start = (int64_t)cta * total / n_ctas;
+    const int64_t end = (int64_t)(cta + 1) * total / n_ctas;
+    if (start >= end) return pl;
+    pl.u0 = (int)(start / T);
+    pl.u1 = (int)((end - 1) / T);
+    pl.k0 = (int)(start % T);
+    pl.k1 = (int)((end - 1) % T + 1);
+    if (pl.u0 == pl.u1 && pl.k0 > 0 && pl.k1 < T) {     // middle piece of one chain
+        pl.middle = 1;
+        pl.n_pre = pl.p1;
+        pl.n_items = pl.n_pre + 1;
+        return pl;
+    }
+    // head piece of chain u1 (starts at tile 0, ends before T); tail piece of chain u0
+    const bool head = (pl.u0 == pl.u1) ? (pl.k0 == 0 && pl.k1 < T) : (pl.k1 < T);
+    const bool tail = pl.k0 > 0;
+    pl.n_pre = head ? 1 + pl.p1 : 0;
+    const int f_first = tail ? pl.u0 + 1 : pl.u0;
+    const int f_last = head ? pl.u1 - 1 : pl.u1;
+    if (f_last >= f_first) {
+        pl.f_lo = f_first;
+        pl.n_full = f_last - f_first + 1;
+    }
+    pl.n_items = pl.n_pre + pl.n_full + (tail ? 1 : 0);
+    return pl;
+}
+
+SSD_HD Item plan_item(const Plan& pl, int i, int T) {
+    if (pl.middle) {
+        if (pl.n_pre > 0 && i == 0) return Item{pl.u0, pl.k0, pl.k1, 1, kInitZero, kFinAgg};
+        return Item{pl.u0, pl.k0, pl.k1, 0, kInitLookback, kFinIncl};
+    }
+    if (i < pl.n_pre) {
+        if (pl.p1 && i == 0) return Item{pl.u1, 0, pl.k1, 1, kInitH0, kFinIncl};
+        return Item{pl.u1, 0, pl.k1, 0, kInitH0, pl.p1 ? kFinNone : kFinIncl};
+    }
+    i -= pl.n_pre;
+    if (i < pl.n_full) return Item{pl.f_lo + i, 0, T, 0, kInitH0, kFinFinal};
+    return Item{pl.u0, pl.k0, (pl.u0 == pl.u1) ? pl.k1 : T, 0, kInitLookback, kFinFinal};
+}
+
+}  // namespace plan
+}  // namespace ssd

@@ -1,0 +1,150 @@
+// Host checks of the tensor-core kernel's work plan (mamba_ssd_scan_05_b300/csrc/tc_plan.cuh):
+// for many (units, tiles per chain, CTAs, state-only-pass mode) it runs make_plan / plan_item
+// for every CTA, exactly as the kernel does, and checks that
+//   1. each CTA's items stay inside its contiguous tile range;
+//   2. every tile of every chain is produced (non state-only) exactly once;
+//   3. a piece that starts at tile 0 starts from the initial state, any other piece looks
+//      back, and the look-back walk over the preceding CTAs' publications reaches an
+//      inclusive state through pieces that end exactly where the next begins;
+//   4. a CTA publishes for one chain only (its flags are per CTA), at most one inclusive state
+//      and one aggregate;
+//   5. every chain ends in exactly one final-state item, at its last tile;
+//   6. a state-only pass covers the same tiles as the piece it precedes.
+// Prints the first violations and exits non-zero if there are any.
+#include <cstdio>
+#include <cstdlib>
+#include <vector>
+
+#include "../mamba_ssd_scan_05_b300/csrc/tc_plan.cuh"
+
+using namespace ssd::plan;
+
+namespace {
+
+int g_fail = 0;
+
+void fail(const char* what, long U, int T, int C, int p1, int cta, long detail) {
+    if (g_fail < 20)
+        std::printf("FAIL %s: U=%ld T=%d C=%d p1=%d cta=%d (%ld)\n", what, U, T, C, p1, cta,
+                    detail);
+    ++g_fail;
+}
+
+struct Pub {
+    int u = -1, k0 = 0, k1 = 0;
+    bool set = false;
+};
+
+void check(long U, int T, int C, int p1) {
+    const long total = U * T;
+    std::vector<int> cover((size_t)total, 0);
+    std::vector<int> finals((size_t)U, 0);
+    std::vector<Pub> incl((size_t)C), agg((size_t)C);
+    struct Look {
+        int cta, u, k0;
+    };
+    std::vector<Look> looks;
+    for (int c = 0; c < C; ++c) {
+        const long start = (long)c * total / C, end = (long)(c + 1) * total / C;
+        const Plan pl = make_plan(U, T, C, p1, c);
+        int pub_unit = -1;
+        for (int i = 0; i < pl.n_items; ++i) {
+            const Item it = plan_item(pl, i, T);
+            if (it.u < 0 || it.u >= U || it.k0 < 0 || it.k1 > T || it.k0 >= it.k1) {
+                fail("item range", U, T, C, p1, c, i);
+                continue;
+            }
+            if ((long)it.u * T + it.k0 < start || (long)it.u * T + it.k1 > end)
+                fail("item outside the CTA range", U, T, C, p1, c, i);
+            if (it.pass1) {
+                // 6: the next item is the full pass over the same tiles
+                if (i + 1 >= pl.n_items) {
+                    fail("state-only pass without its piece", U, T, C, p1, c, i);
+                } else {
+                    const Item nx = plan_item(pl, i + 1, T);
+                    if (nx.u != it.u || nx.k0 != it.k0 || nx.k1 != it.k1 || nx.pass1)
+                        fail("state-only pass and its piece differ", U, T, C, p1, c, i);
+                }
+            } else {
+                for (int k = it.k0; k < it.k1; ++k) ++cover[(size_t)it.u * T + k];
+            }
+            // 3: initial state versus look-back
+            if (it.init == kInitH0 && it.k0 != 0) fail("initial state mid-chain", U, T, C, p1, c, i);
+            if (it.init == kInitLookback) {
+                if (it.k0 == 0) fail("look-back at a chain start", U, T, C, p1, c, i);
+                looks.push_back({c, it.u, it.k0});
+            }
+            if (it.init == kInitZero && !it.pass1)
+                fail("zero start on a full pass", U, T, C, p1, c, i);
+            // 4, 5: publications and final states
+            if (it.fin == kFinIncl || it.fin == kFinAgg) {
+                if (pub_unit >= 0 && pub_unit != it.u)
+                    fail("publishes for two chains", U, T, C, p1, c, i);
+                pub_unit = it.u;
+                Pub& pb = (it.fin == kFinIncl) ? incl[c] : agg[c];
+                if (pb.set) fail("two publications of one kind", U, T, C, p1, c, i);
+                pb.set = true;
+                pb.u = it.u;
+                pb.k0 = it.k0;
+                pb.k1 = it.k1;
+                if (it.k1 == T) fail("publishes at a chain end", U, T, C, p1, c, i);
+            }
+            if (it.fin == kFinFinal) {
+                if (it.pass1 || it.k1 != T) fail("final state not at the chain end", U, T, C, p1, c, i);
+                ++finals[(size_t)it.u];
+            }
+        }
+    }
+    for (long t = 0; t < total; ++t)
+        if (cover[(size_t)t] != 1) {
+            fail("tile not produced exactly once", U, T, C, p1, -1, t);
+            break;
+        }
+    for (long u = 0; u < U; ++u)
+        if (finals[(size_t)u] != 1) {
+            fail("chain without exactly one final state", U, T, C, p1, -1, u);
+            break;
+        }
+    // 3: the look-back walk (kind 1 = inclusive state: stop; kind 2 = aggregate: go on)
+    for (const Look& lk : looks) {
+        int pos = lk.k0;
+        bool done = false;
+        for (int jp = lk.cta - 1; jp >= 0 && !done; --jp) {
+            const Pub& in = incl[jp];
+            const Pub& ag = agg[jp];
+            if (in.set && in.u == lk.u && in.k1 == pos) {
+                done = true;                  // the walk may take the inclusive state ...
+            } else if (ag.set && ag.u == lk.u && ag.k1 == pos) {
+                pos = ag.k0;                  // ... or compose the aggregate and go on
+            } else {
+                fail("look-back finds no state ending at its start", U, T, C, p1, lk.cta, jp);
+                break;
+            }
+            // a CTA that has both publishes them over the same tiles
+            if (in.set && ag.set && (in.k0 != ag.k0 || in.k1 != ag.k1))
+                fail("aggregate and inclusive state differ", U, T, C, p1, jp, 0);
+        }
+        if (!done && pos > 0) fail("look-back runs out of CTAs", U, T, C, p1, lk.cta, pos);
+    }
+}
+
+}  // namespace
+
+int main() {
+    const long units[] = {1, 2, 3, 5, 8, 24, 80, 192, 320, 1000, 10240};
+    const int tiles[] = {1, 2, 3, 7, 16, 32, 129, 1024};
+    const int ctas[] = {1, 2, 3, 7, 148, 256};
+    long cases = 0;
+    for (long U : units)
+        for (int T : tiles)
+            for (int C0 : ctas) {
+                const long total = U * T;
+                const int C = (int)(C0 < total ? C0 : total);   // the launcher's clamp
+                for (int p1 = 0; p1 < 2; ++p1) {
+                    check(U, T, C, p1);
+                    ++cases;
+                }
+            }
+    std::printf("%ld plans checked, %d violations\n", cases, g_fail);
+    return g_fail ? 1 : 0;
+}
