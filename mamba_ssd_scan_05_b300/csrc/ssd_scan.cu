@@ -384,6 +384,6 @@ const char* ssd_scan_strerror(int code) {
     }
 }
 
-int ssd_scan_version(void) { return 100; }
+int ssd_scan_version(void) { return 200; }   // 0.2.0: + step, conv1d, gated RMSNorm, varlen
 
 }  // extern "C"

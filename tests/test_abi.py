@@ -44,7 +44,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_strerror(lib):
     import mamba_ssd_scan_05_b300 as m
-    assert m.ssd_scan_version() >= 100
+    assert m.ssd_scan_version() >= 200
     for code in range(6):
         assert m.ssd_scan_strerror(code)
     assert "unknown" in m.ssd_scan_strerror(99)
