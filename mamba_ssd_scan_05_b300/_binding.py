@@ -80,6 +80,8 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_scan_fwd_varlen.restype = i32
         lib.ssd_scan_get_status.argtypes = [vp, vp]
         lib.ssd_scan_get_status.restype = i32
+        lib.ssd_scan_set_wait_cycles.argtypes = [ctypes.c_int64]
+        lib.ssd_scan_set_wait_cycles.restype = ctypes.c_int64
         lib.ssd_scan_strerror.argtypes = [i32]
         lib.ssd_scan_strerror.restype = ctypes.c_char_p
         lib.ssd_scan_version.argtypes = []
@@ -154,7 +156,8 @@ def ssd_scan_fwd(x, dt, A, B, C, D=None, initial_state=None, chunk_size: int = 2
     """y, final_state = scan(x, dt, A, B, C, D, initial_state) on x's CUDA device.
 
     Enqueued on torch's current stream; outputs (and the workspace, unless given) are
-    allocated with torch.  Raises SSDError on any non-zero return code.
+    allocated with torch.  A given workspace smaller than ssd_scan_workspace_bytes raises
+    SSDError(SSD_ERR_WORKSPACE).  Raises SSDError on any non-zero return code.
     """
     _check_inputs(x, dt, A, B, C, D, initial_state)
     if not x.is_cuda:
@@ -171,7 +174,9 @@ def ssd_scan_fwd(x, dt, A, B, C, D=None, initial_state=None, chunk_size: int = 2
     if need == 0:
         rc = lib.ssd_scan_resolve_path(ctypes.byref(dims), int(chunk_size), int(path))
         raise SSDError(-rc if rc < 0 else SSD_ERR_INVALID, "ssd_scan_workspace_bytes")
-    if workspace is None or workspace.numel() < need:
+    # a workspace the caller passes is used as it is: one that is too small comes back from
+    # the library as SSD_ERR_WORKSPACE (replacing it would hide the call's status word)
+    if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     args = (ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
             _ptr(initial_state), int(chunk_size), _ptr(y), _ptr(final_state), _ptr(workspace),
@@ -226,7 +231,7 @@ def ssd_scan_fwd_varlen(x, dt, A, B, C, cu_seqlens, D=None, initial_states=None,
                                                int(path))
     if need == 0:
         raise SSDError(SSD_ERR_INVALID, "ssd_scan_varlen_workspace_bytes")
-    if workspace is None or workspace.numel() < need:
+    if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     rc = lib.ssd_scan_fwd_varlen(ctypes.byref(dims), cu, nseq, _ptr(x), _ptr(dt), _ptr(A),
                                  _ptr(B), _ptr(C), _ptr(D), _ptr(initial_states),
@@ -331,6 +336,12 @@ def ssd_scan_get_status(workspace, device=None) -> int:
     return lib.ssd_scan_get_status(_ptr(workspace), _stream_handle(device or workspace.device))
 
 
+def ssd_scan_set_wait_cycles(cycles: int) -> int:
+    """Limit of each device-side wait of the tensor-core kernels, in SM cycles (<= 0: the
+    default).  Process-wide; returns the previous limit."""
+    return load_library().ssd_scan_set_wait_cycles(int(cycles))
+
+
 def ssd_scan_host_arena_bytes(dims: ssd_dims, chunk_size: int) -> int:
     return load_library().ssd_scan_host_arena_bytes(ctypes.byref(dims), int(chunk_size))
 
@@ -340,7 +351,8 @@ def ssd_scan_fwd_host(x, dt, A, B, C, D=None, initial_state=None, chunk_size: in
     """The host-buffer entry point: CPU tensors in and out (pinned memory recommended).
 
     Copies in, scans and copies out on the current stream of ``device`` and synchronises it
-    before returning.  ``arena`` (a CUDA uint8 tensor) is reused when given and large enough.
+    before returning.  ``arena`` (a CUDA uint8 tensor) is used when given; one smaller than
+    ssd_scan_host_arena_bytes raises SSDError(SSD_ERR_WORKSPACE).
     """
     _check_inputs(x, dt, A, B, C, D, initial_state)
     if x.is_cuda:
@@ -357,7 +369,7 @@ def ssd_scan_fwd_host(x, dt, A, B, C, D=None, initial_state=None, chunk_size: in
     need = lib.ssd_scan_host_arena_bytes(ctypes.byref(dims), int(chunk_size))
     if need == 0:
         raise SSDError(SSD_ERR_INVALID, "ssd_scan_host_arena_bytes")
-    if arena is None or arena.numel() < need:
+    if arena is None:
         arena = torch.empty(need, dtype=torch.uint8, device=device)
     stream = _stream_handle(device)
     rc = lib.ssd_scan_fwd_host(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),

@@ -52,6 +52,14 @@ extern "C" int ssd_scan_fwd_noalloc(const ssd_dims* dims, const void* x, const v
         return r < 0 ? -r : SSD_ERR_INVALID;
     }
     if (need > kScratchBytes) return SSD_ERR_WORKSPACE;
+    // the scratch address is the current device's: the stream must belong to that device
+    if (stream) {
+        int dev = -1, sdev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess)
+            return SSD_ERR_CUDA;
+        if (dev != sdev) return SSD_ERR_INVALID;
+    }
     void* scratch = nullptr;
     const int rc = scratch_address(&scratch);
     if (rc != SSD_OK) return rc;

@@ -1,17 +1,17 @@
 """The no-allocation entry point (ssd_scan_fwd_noalloc) through the C ABI.
 
 It serves callers that cannot allocate device memory: they pass inputs and outputs only and the
-library uses its own fixed device buffer.  Its results must match the regular entry point's on
-two calls in a row (the second call must not see anything left over from the first), and an
-oversized problem must be refused before anything runs.  This file is named so pytest collects
-it last.
+library uses its own fixed device buffer.  On two calls in a row -- the second one a smaller
+problem, so that it runs over what the first left in the shared buffer -- its results must
+match the CPU oracle and the regular entry point's, and an oversized problem must be refused
+before anything runs.  This file is named so pytest collects it last.
 """
 import ctypes
 
 import pytest
 import torch
 
-from gpu_helpers import TOL, assert_close, to_device
+from gpu_helpers import TOL, assert_close, check_against_oracle, to_device
 from mamba_ssd_scan_05_b300 import SSD_PATH_CHUNKED, make_dims, ssd_scan_fwd, workloads
 from mamba_ssd_scan_05_b300._binding import load_library
 
@@ -47,15 +47,17 @@ def _call(fn, dev, chunk):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_noalloc_matches_regular_entry_point_twice(dtype):
+def test_noalloc_matches_oracle_and_regular_entry_point_twice(dtype):
     fn = _noalloc_fn()
-    # two different input sets of one shape, scanned back to back
-    for call, seed in enumerate((11, 12)):
-        inp = workloads.make_shape_inputs(2, 700, 4, 64, 128, 2, dtype, seed=seed,
-                                          h0_mode="normal", d_mode="normal")
+    # two input sets scanned back to back, the second smaller than the first
+    shapes = [(2, 700, 4, 64, 128, 2), (1, 333, 2, 64, 128, 1)]
+    for call, (seed, shape) in enumerate(zip((11, 12), shapes)):
+        inp = workloads.make_shape_inputs(*shape, dtype, seed=seed, h0_mode="normal",
+                                          d_mode="normal")
         dev = to_device(inp)
         rc, y, hT = _call(fn, dev, 128)
         assert rc == SSD_OK, f"call {call}: return code {rc}"
+        check_against_oracle(inp, y, hT, what=f"no-alloc call {call}")
         y_ref, h_ref = ssd_scan_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"],
                                     dev["D"], dev["h0"], chunk_size=128)
         torch.cuda.synchronize()
