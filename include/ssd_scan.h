@@ -146,6 +146,8 @@ int ssd_scan_fwd_host(const ssd_dims* dims,
  *   - Problems whose scratch (ssd_scan_workspace_bytes(dims, chunk_size, SSD_PATH_CHUNKED))
  *     exceeds SSD_NOALLOC_SCRATCH_BYTES are rejected with SSD_ERR_WORKSPACE before anything is
  *     enqueued.  Other errors as ssd_scan_fwd.
+ *   - The scratch is the one of the CURRENT device: `stream` must belong to it (a stream of
+ *     another device is rejected with SSD_ERR_INVALID).
  *   - The first call on each device looks up the buffer's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make that first call
  *     before any stream capture.
@@ -277,6 +279,16 @@ int ssd_gated_rmsnorm_fwd(int64_t rows, int64_t dim, int64_t group_size, int32_t
  * 4 bytes).  Returns SSD_OK, SSD_ERR_TIMEOUT if a bounded device wait gave up in a call that
  * used this workspace, or SSD_ERR_CUDA if synchronisation or the read failed. */
 int ssd_scan_get_status(void* workspace, void* stream);
+
+/* Limit, in SM clock cycles, of every device-side wait of the tensor-core kernels (a barrier
+ * between warp roles, or the hand-off of a running state between thread blocks).  A wait that
+ * reaches it makes the kernel stop, record SSD_ERR_TIMEOUT in the workspace status word
+ * (ssd_scan_get_status) and return; the context stays usable.  cycles <= 0 restores the
+ * default, 2^32 cycles (about 2 s at the B300's maximum SM clock).  The setting is process-wide
+ * and applies to launches enqueued after the call; a limit far below a wait's normal length
+ * makes calls fail with SSD_ERR_TIMEOUT, which is what tests of the timeout path use it for.
+ * Returns the previous limit. */
+int64_t ssd_scan_set_wait_cycles(int64_t cycles);
 
 /* Static description of a return code. */
 const char* ssd_scan_strerror(int code);

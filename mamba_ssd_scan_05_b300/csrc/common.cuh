@@ -104,7 +104,11 @@ struct NormArgs {
 };
 int norm_launch(const NormArgs& a);
 
-// Tensor-core path (tc.cu).
+// Tensor-core path (tc.cu; the d_state 128 kernel in tc128.cu).
+// Cycles a single device-side wait of the tensor-core kernels may take (process-wide setting,
+// ssd_scan_set_wait_cycles).
+long long tc_wait_budget();
+int tc128_launch(const ScanArgs& a);
 size_t tc_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t P, int64_t N, int Q);
 bool tc_supports(int32_t dtype, int64_t P, int64_t N, int Q);
 int tc_launch(const ScanArgs& a);

@@ -87,5 +87,17 @@ SSD_HD Item plan_item(const Plan& pl, int i, int T) {
     return Item{pl.u0, pl.k0, (pl.u0 == pl.u1) ? pl.k1 : T, 0, kInitLookback, kFinFinal};
 }
 
+// The look-back's choice for predecessor CTA jp of a range that continues chain u: true takes
+// jp's aggregate and goes on to jp - 1, false takes jp's inclusive state and stops.  With the
+// state-only pass, a CTA whose range starts inside chain u holds a middle piece of it, whose
+// aggregate that pass publishes early; the CTA whose range starts at or before the chain's
+// first tile holds the head piece.  Without it, every piece publishes its inclusive state.
+// Fixed by the plan, so every run combines the same states in the same order.
+SSD_HD bool lookback_uses_aggregate(int64_t n_units, int n_tiles, int n_ctas, int pass1_mode,
+                                    int jp, int u) {
+    const int64_t total = n_units * n_tiles;
+    return pass1_mode != 0 && (int64_t)jp * total / n_ctas > (int64_t)u * n_tiles;
+}
+
 }  // namespace plan
 }  // namespace ssd

@@ -71,6 +71,51 @@ def check_against_oracle(inp_cpu: dict, y_dev, hT_dev, heads=None, use_D=True, u
     return r
 
 
+def check_all_heads(inp_cpu: dict, y_dev, hT_dev, what="", heads_per_batch: int = 16,
+                    use_D=True, use_h0=True):
+    """Compare every (b, h) head with the oracle, a batch of heads at a time.
+
+    The metrics are the global ones of ``assert_close`` (max|dy| / max|y_ref| and
+    sum|dy| / sum|y_ref| over all heads), accumulated batch by batch so that the float64
+    copies of a large workload never sit in host memory all at once.  Returns the two metrics
+    for y and for the final state.
+    """
+    dt_name = dtype_name(inp_cpu["x"].dtype)
+    bsz, _, H, _ = inp_cpu["x"].shape
+    D = inp_cpu["D"] if use_D else None
+    h0 = inp_cpu["h0"] if use_h0 else None
+    heads = [(b, h) for b in range(bsz) for h in range(H)]
+    acc = {"y": [0.0, 0.0, 0.0, 0.0], "final_state": [0.0, 0.0, 0.0, 0.0]}
+    for i in range(0, len(heads), heads_per_batch):
+        part = heads[i:i + heads_per_batch]
+        y_ref, h_ref = oracle.scan(inp_cpu["x"], inp_cpu["dt"], inp_cpu["A"], inp_cpu["B"],
+                                   inp_cpu["C"], D, h0, heads=part)
+        got_y = torch.stack([y_dev[b, :, h, :] for b, h in part]).double().cpu().numpy()
+        pairs = [("y", got_y, y_ref)]
+        if hT_dev is not None:
+            got_h = torch.stack([hT_dev[b, h] for b, h in part]).double().cpu().numpy()
+            pairs.append(("final_state", got_h, h_ref))
+        for name, got, ref in pairs:
+            assert np.all(np.isfinite(got)), f"{what} {name}: non-finite values"
+            d = np.abs(got - ref)
+            a = acc[name]
+            a[0] = max(a[0], float(d.max(initial=0.0)))
+            a[1] = max(a[1], float(np.abs(ref).max(initial=0.0)))
+            a[2] += float(d.sum())
+            a[3] += float(np.abs(ref).sum())
+    tmax, tmean = TOL[dt_name]
+    out = {}
+    for name, (dmax, rmax, dsum, rsum) in acc.items():
+        if name == "final_state" and hT_dev is None:
+            continue
+        mx = dmax / rmax if rmax > 0 else dmax
+        mean = dsum / rsum if rsum > 0 else dsum
+        assert mx <= tmax, f"{what} {name}: max rel err {mx:.3e} > {tmax:.0e}"
+        assert mean <= tmean, f"{what} {name}: mean rel err {mean:.3e} > {tmean:.0e}"
+        out[name] = (mx, mean)
+    return out
+
+
 @functools.lru_cache(maxsize=2)
 def workload_inputs(idx: int) -> dict:
     return workloads.make_inputs(workloads.WORKLOADS[idx])

@@ -4,8 +4,9 @@
 //   1. each CTA's items stay inside its contiguous tile range;
 //   2. every tile of every chain is produced (non state-only) exactly once;
 //   3. a piece that starts at tile 0 starts from the initial state, any other piece looks
-//      back, and the look-back walk over the preceding CTAs' publications reaches an
-//      inclusive state through pieces that end exactly where the next begins;
+//      back, and the look-back walk over the preceding CTAs' publications, taking from each
+//      the publication lookback_uses_aggregate names, reaches an inclusive state through
+//      pieces that end exactly where the next begins;
 //   4. a CTA publishes for one chain only (its flags are per CTA), at most one inclusive state
 //      and one aggregate;
 //   5. every chain ends in exactly one final-state item, at its last tile;
@@ -105,20 +106,28 @@ void check(long U, int T, int C, int p1) {
             fail("chain without exactly one final state", U, T, C, p1, -1, u);
             break;
         }
-    // 3: the look-back walk (kind 1 = inclusive state: stop; kind 2 = aggregate: go on)
+    // 3: the look-back walk, with the kernel's rule for which publication each predecessor
+    // contributes (aggregate: compose and go on; inclusive state: stop)
     for (const Look& lk : looks) {
         int pos = lk.k0;
         bool done = false;
         for (int jp = lk.cta - 1; jp >= 0 && !done; --jp) {
             const Pub& in = incl[jp];
             const Pub& ag = agg[jp];
-            if (in.set && in.u == lk.u && in.k1 == pos) {
-                done = true;                  // the walk may take the inclusive state ...
-            } else if (ag.set && ag.u == lk.u && ag.k1 == pos) {
-                pos = ag.k0;                  // ... or compose the aggregate and go on
+            if (!lookback_uses_aggregate(U, T, C, p1, jp, lk.u)) {
+                if (!(in.set && in.u == lk.u && in.k1 == pos)) {
+                    fail("look-back wants an inclusive state that is not there", U, T, C, p1,
+                         lk.cta, jp);
+                    break;
+                }
+                done = true;
             } else {
-                fail("look-back finds no state ending at its start", U, T, C, p1, lk.cta, jp);
-                break;
+                if (!(ag.set && ag.u == lk.u && ag.k1 == pos)) {
+                    fail("look-back wants an aggregate that is not there", U, T, C, p1, lk.cta,
+                         jp);
+                    break;
+                }
+                pos = ag.k0;
             }
             // a CTA that has both publishes them over the same tiles
             if (in.set && ag.set && (in.k0 != ag.k0 || in.k1 != ag.k1))

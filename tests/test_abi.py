@@ -145,3 +145,13 @@ def test_varlen_workspace_checks_offsets(lib):
     assert m.ssd_scan_varlen_workspace_bytes(d, [0, 100, 299], 128) == 0      # wrong total
     assert m.ssd_scan_varlen_workspace_bytes(d, [0, 200, 100, 300], 128) == 0  # decreasing
     assert m.ssd_scan_varlen_workspace_bytes(dims(b=2, L=300), [0, 300], 128) == 0  # batch != 1
+
+
+def test_wait_limit_setter_round_trip(lib):
+    import mamba_ssd_scan_05_b300 as m
+    m.ssd_scan_set_wait_cycles(0)
+    # the call returns the previous limit; <= 0 restores the default (2^32 cycles)
+    assert m.ssd_scan_set_wait_cycles(0) == 1 << 32
+    assert m.ssd_scan_set_wait_cycles(500) == 1 << 32
+    assert m.ssd_scan_set_wait_cycles(-1) == 500
+    assert m.ssd_scan_set_wait_cycles(0) == 1 << 32

@@ -42,6 +42,9 @@ CONV = [
     (1, 40, 8, 5, "bf16", True, False, True),
     (1, 31, 20, 6, "f32", True, True, True),
     (1, 65, 32, 7, "bf16", False, True, True),
+    # several 64-token blocks with a ragged end; 96- and 128-thread blocks over the channels
+    (1, 300, 768, 4, "bf16", True, True, True),
+    (2, 129, 1024, 4, "f32", False, True, True),
 ]
 
 

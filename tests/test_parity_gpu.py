@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (TOL, assert_close, check_against_oracle, run_gpu, sample_heads,
+from gpu_helpers import (TOL, assert_close, check_against_oracle, check_all_heads, run_gpu,
                          to_device, workload_inputs)
 from mamba_ssd_scan_05_b300 import (SSD_PATH_AUTO, SSD_PATH_CHUNKED, SSD_PATH_TC, SSDError,
                                     make_dims, ssd_scan_fwd, ssd_scan_fwd_host,
@@ -18,7 +18,7 @@ def available_paths(inp, chunk):
     return [p for p in (SSD_PATH_CHUNKED, SSD_PATH_TC) if ssd_scan_resolve_path(dims, chunk, p) == p]
 
 
-# ---- the five workloads at full size (sampled heads for the large ones) --------------------
+# ---- the five workloads at full size, every (b, h) head against the oracle ------------------
 
 @pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
 def test_workload_full_size(idx):
@@ -26,8 +26,7 @@ def test_workload_full_size(idx):
     inp = workload_inputs(idx)
     dev = to_device(inp)
     y, hT = run_gpu(dev, w.chunk)
-    heads = None if idx == 0 else sample_heads(w.batch, w.nheads, k=4, seed=idx)
-    check_against_oracle(inp, y, hT, heads=heads, what=w.name)
+    check_all_heads(inp, y, hT, what=w.name)
 
 
 # ---- small cases: several tiles, ragged tails, every kernel family that takes the shape ----

@@ -31,6 +31,9 @@ MUTANTS = {
     # the tail piece starting from the initial state instead of looking back
     "tail_no_look_back": ("return Item{pl.u0, pl.k0, (pl.u0 == pl.u1) ? pl.k1 : T, 0, kInitLookback, kFinFinal};",
                           "return Item{pl.u0, pl.k0, (pl.u0 == pl.u1) ? pl.k1 : T, 0, kInitH0, kFinFinal};"),
+    # the look-back rule taking an aggregate also from the head piece's CTA
+    "lookback_rule": ("return pass1_mode != 0 && (int64_t)jp * total / n_ctas > (int64_t)u * n_tiles;",
+                      "return pass1_mode != 0 && (int64_t)jp * total / n_ctas >= (int64_t)u * n_tiles;"),
 }
 
 
