@@ -68,7 +68,8 @@ def load_peaks():
 
 # Source files each profiled kernel is built from (a traffic record is valid for these bytes).
 KERNEL_SOURCES = {
-    "ssd_tc_kernel": ("tc.cu", "tc_plan.cuh", "tc_ptx.cuh", "common.cuh"),
+    "ssd_tc_ws_kernel": ("tc128.cu", "tc_common.cuh", "tc_plan.cuh", "tc_ptx.cuh", "common.cuh"),
+    "ssd_tc_kernel": ("tc.cu", "tc_common.cuh", "tc_plan.cuh", "tc_ptx.cuh", "common.cuh"),
     "step_kernel_vec": ("step.cu", "common.cuh"),
     "conv_kernel": ("block.cu", "common.cuh"),
     "norm_kernel": ("block.cu", "common.cuh"),
@@ -604,10 +605,16 @@ def main():
     ap.add_argument("--path", type=int, default=-1, help="kernel family (-1 auto, 0 chunked, 1 tc)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--also", default=None,
+                    help="comma-separated workload indices measured after --workload and reported "
+                         "in the same line under other_workloads (default: 3 when --workload is "
+                         "2, else none; '' for none)")
     ap.add_argument("--op", choices=["scan", "step", "conv", "norm", "varlen"], default="scan",
                     help="scan: the forward scan (default); step: the recurrent decode step; "
                          "conv / norm: the block steps before / after the scan")
     args = ap.parse_args()
+    if args.also is None:
+        args.also = "3" if args.workload == 2 else ""
     if args.warmup < 3:
         args.warmup = 3
     if args.op != "scan":
@@ -628,18 +635,48 @@ def main():
 
     import torch
     import torch.distributed as dist
-    import mamba_ssd_scan_05_b300 as m
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if ws > 1:
         dist.init_process_group("nccl", device_id=dev)
+    line = measure_scan(args, w, dev, ws, rank, local)
+    # the other workloads the performance target names (the 128K-token scan beside the
+    # 2.7B-shaped layer), measured the same way and reported inside the same line
+    also = [int(v) for v in args.also.split(",") if v.strip()] if args.also else []
+    extra = []
+    for idx in also:
+        if idx == args.workload:
+            continue
+        sub = measure_scan(args, workloads.WORKLOADS[idx], dev, ws, rank, local)
+        if sub is not None:
+            extra.append({k: sub[k] for k in ("value", "unit", "ms_per_step", "config",
+                                              "tflops_effective", "roofline", "cpu_baseline",
+                                              "e2e", "gpu_launches", "clocks", "device_status",
+                                              "per_call_ms")})
+    if rank == 0:
+        if extra:
+            line["other_workloads"] = extra
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
 
-    # inputs: enough distinct sets that consecutive steps never find theirs in L2
+
+def measure_scan(args, w, dev, ws, rank, local):
+    """Time --steps ssd_scan_fwd calls on workload w (after --warmup); the bench line's fields
+    for it on rank 0, None on the other ranks."""
+    import torch
+    import torch.distributed as dist
+    import mamba_ssd_scan_05_b300 as m
+    from mamba_ssd_scan_05_b300 import workloads
+
+    # inputs: enough distinct sets that consecutive steps never find theirs in L2 (one set
+    # when a set alone is several times larger than L2)
     inp = workloads.make_inputs(w)
     with_h0 = inp["h0"] is not None
     set_bytes = algorithmic_bytes(w, with_h0)
-    n_sets = max(2, math.ceil(3 * L2_BYTES / set_bytes))
+    n_sets = 1 if set_bytes >= 8 * L2_BYTES else max(2, math.ceil(3 * L2_BYTES / set_bytes))
     sets = []
     for s in range(n_sets):
         src = inp if s == 0 else workloads.make_inputs(w, seed=w.seed + 7919 * s)
@@ -661,7 +698,6 @@ def main():
         m.ssd_scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"],
                        chunk_size=w.chunk, path=args.path, y=d["y"], final_state=d["hT"],
                        workspace=workspace)
-
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
@@ -740,9 +776,7 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     if rank != 0:
-        if ws > 1:
-            dist.destroy_process_group()
-        return 0
+        return None
 
     peaks, peak_src = load_peaks()
     nbytes = algorithmic_bytes(w, with_h0)
@@ -751,7 +785,8 @@ def main():
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
-    kernel = {m.SSD_PATH_CHUNKED: "chunk_output_kernel", m.SSD_PATH_TC: "ssd_tc_kernel"}[path]
+    kernel = {m.SSD_PATH_CHUNKED: "chunk_output_kernel",
+              m.SSD_PATH_TC: "ssd_tc_ws_kernel" if w.dstate == 128 else "ssd_tc_kernel"}[path]
     traffic = committed_traffic(kernel, w.name)
     if bound == "hbm":
         achieved, peak, unit = nbytes / avg_call_s / 1e9, peaks["hbm_gbs"], "GB/s"
@@ -790,10 +825,7 @@ def main():
         "per_call_ms": {"median": statistics.median(call_ms), "min": min(call_ms),
                         "max": max(call_ms)},
     }
-    print(json.dumps(line), flush=True)
-    if ws > 1:
-        dist.destroy_process_group()
-    return 0
+    return line
 
 
 if __name__ == "__main__":
