@@ -505,6 +505,110 @@ def run_block(args, op, local):
     return 0
 
 
+def run_gated(args, local):
+    """The scan followed by the gated RMSNorm of its output on the 2.7B-shaped layer, groups of
+    one head (64 features): the fused form (ssd_scan_fwd_gated: the norm in the scan kernel's
+    epilogue, y never written) against the two-kernel form (ssd_scan_fwd, then
+    ssd_gated_rmsnorm_fwd reading y back).  Each timed call replays a CUDA graph."""
+    import torch
+    import mamba_ssd_scan_05_b300 as m
+    from mamba_ssd_scan_05_b300 import workloads
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workloads.WORKLOADS[2]
+    group = w.headdim
+    sets = []
+    n_sets = 2
+    for s_ in range(n_sets):
+        src = workloads.make_inputs(w, seed=w.seed + 7919 * s_)
+        d = {k: (None if v is None else v.to(dev)) for k, v in src.items()}
+        g = torch.Generator().manual_seed(77 + s_)
+        d["z"] = torch.randn(d["x"].shape, generator=g).to(torch.bfloat16).to(dev)
+        d["out"] = torch.empty_like(d["x"])
+        d["y"] = torch.empty_like(d["x"])
+        d["hT"] = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32,
+                              device=dev)
+        sets.append(d)
+    nw = (1.0 + 0.1 * torch.randn(w.nheads * w.headdim, generator=torch.Generator().manual_seed(5))).float().to(dev)
+    dims = m.make_dims(sets[0]["x"], sets[0]["B"])
+    ws_g = torch.empty(m.ssd_scan_gated_workspace_bytes(dims, w.chunk, group), dtype=torch.uint8,
+                       device=dev)
+    ws_s = torch.empty(m.ssd_scan_workspace_bytes(dims, w.chunk), dtype=torch.uint8, device=dev)
+
+    def fused(i):
+        d = sets[i % n_sets]
+        m.ssd_scan_fwd_gated(d["x"], d["dt"], d["A"], d["B"], d["C"], d["z"], d["D"], d["h0"],
+                             nw, group_size=group, chunk_size=w.chunk, out=d["out"],
+                             final_state=d["hT"], workspace=ws_g)
+
+    def unfused(i):
+        d = sets[i % n_sets]
+        m.ssd_scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"],
+                       chunk_size=w.chunk, y=d["y"], final_state=d["hT"], workspace=ws_s)
+        F = w.nheads * w.headdim
+        m.ssd_gated_rmsnorm_fwd(d["y"].view(-1, F), d["z"].view(-1, F), nw, group_size=group,
+                                out=d["out"].view(-1, F))
+
+    def time_graphs(fn):
+        for i in range(args.warmup):
+            fn(i)
+        torch.cuda.synchronize(dev)
+        graphs = []
+        for i in range(n_sets):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                fn(i)
+            graphs.append(gr)
+        for i in range(args.warmup):
+            graphs[i % n_sets].replay()
+        torch.cuda.synchronize(dev)
+        stream = torch.cuda.current_stream(dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        ev[0].record(stream)
+        for i in range(args.steps):
+            graphs[i % n_sets].replay()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+        return ev[0].elapsed_time(ev[-1]) / args.steps, per
+
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)
+    wall0 = time.time()
+    ms_f, per_f = time_graphs(fused)
+    ms_u, _ = time_graphs(unfused)
+    wall1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    peaks, peak_src = load_peaks()
+    y_bytes = 2 * w.batch * w.seqlen * w.nheads * w.headdim
+    nbytes = algorithmic_bytes(w, sets[0]["h0"] is not None) + y_bytes + 4 * nw.numel()   # + z
+    avg_s = statistics.mean(per_f) / 1e3
+    achieved = nbytes / avg_s / 1e9
+    line = {
+        "metric": "SSD scan + gated RMSNorm tokens/s on 1 B300; % of roofline (HBM)",
+        "value": w.tokens / (ms_f / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_f, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, {"op": "gated", "group_size": group,
+                                      "l2": f"{n_sets} rotating input sets larger than L2",
+                                      "parallelism": "replicas x1"}),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peak_src}", "algorithmic_bytes": nbytes,
+                     "kernel": "ssd_tc128_kernel (gated instance)",
+                     "timed": "one ssd_scan_fwd_gated call (CUDA graph replay)"},
+        "unfused": {"ms_per_step": ms_u, "value": w.tokens / (ms_u / 1e3),
+                    "extra_bytes": 2 * y_bytes,
+                    "what": "ssd_scan_fwd then ssd_gated_rmsnorm_fwd (y written and read back)"},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(wall0, wall1),
+        "cpu_baseline": None, "e2e": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_varlen(args, local):
     """The scan over a packed batch of variable-length sequences (ssd_scan_fwd_varlen)."""
     import torch
@@ -609,9 +713,11 @@ def main():
                     help="comma-separated workload indices measured after --workload and reported "
                          "in the same line under other_workloads (default: 3 when --workload is "
                          "2, else none; '' for none)")
-    ap.add_argument("--op", choices=["scan", "step", "conv", "norm", "varlen"], default="scan",
+    ap.add_argument("--op", choices=["scan", "step", "conv", "norm", "varlen", "gated"],
+                    default="scan",
                     help="scan: the forward scan (default); step: the recurrent decode step; "
-                         "conv / norm: the block steps before / after the scan")
+                         "conv / norm: the block steps before / after the scan; gated: the scan "
+                         "with the gated RMSNorm fused, against scan + norm")
     args = ap.parse_args()
     if args.also is None:
         args.also = "3" if args.workload == 2 else ""
@@ -625,6 +731,8 @@ def main():
             return run_step(args, ws, rank, local)
         if args.op == "varlen":
             return run_varlen(args, local)
+        if args.op == "gated":
+            return run_gated(args, local)
         return run_block(args, args.op, local)
 
     from mamba_ssd_scan_05_b300 import workloads

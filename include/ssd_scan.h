@@ -275,6 +275,35 @@ int ssd_gated_rmsnorm_fwd(int64_t rows, int64_t dim, int64_t group_size, int32_t
                           const void* y, const void* z, const float* weight, float eps,
                           void* out, void* stream);
 
+/*
+ * ssd_scan_fwd_gated -- the scan followed by the gated RMSNorm of its output, the block's next
+ * step (Qiita "Mamba-2 / SSD" article, section 4.2, step 4: y = rmsnorm(y) * silu(z)):
+ *
+ *     out[b,t,f] = y[b,t,f] / sqrt(mean_{f' in group(f)} y[b,t,f']^2 + eps) * w[f] * silu(z[b,t,f])
+ *
+ * with y the scan of ssd_scan_fwd, f = h * headdim + p the feature index of a token, and groups
+ * of group_size consecutive features.
+ *
+ *   - z: [batch, seqlen, nheads, headdim] of the element type (16-byte aligned); out: the same
+ *     (written; y itself is not).  norm_weight: [nheads * headdim] float32 (or NULL for ones);
+ *     eps >= 0.  group_size divides nheads * headdim.  Everything else as ssd_scan_fwd.
+ *   - When the problem runs on the tensor-core kernel for d_state 128 and group_size is 8, 16,
+ *     32 or 64 (a group then lies inside one head's 64-feature slice), the norm is applied in
+ *     the scan kernel's epilogue from the float32 y, and y never goes to memory (norm_weight
+ *     must then be 16-byte aligned).  Otherwise the scan writes y into the workspace and the
+ *     gated RMSNorm kernel (ssd_gated_rmsnorm_fwd) reads it.
+ *   - workspace: at least ssd_scan_gated_workspace_bytes (0 on invalid input).  Errors and
+ *     status word as ssd_scan_fwd.
+ */
+size_t ssd_scan_gated_workspace_bytes(const ssd_dims* dims, int chunk_size, int64_t group_size);
+int ssd_scan_fwd_gated(const ssd_dims* dims,
+                       const void* x, const void* dt, const float* A,
+                       const void* B, const void* C, const float* D,
+                       const float* initial_state, int chunk_size,
+                       const void* z, const float* norm_weight, float eps, int64_t group_size,
+                       void* out, float* final_state,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word of `workspace` (the first
  * 4 bytes).  Returns SSD_OK, SSD_ERR_TIMEOUT if a bounded device wait gave up in a call that
  * used this workspace, or SSD_ERR_CUDA if synchronisation or the read failed. */

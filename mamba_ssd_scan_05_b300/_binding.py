@@ -80,6 +80,11 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_scan_fwd_varlen.restype = i32
         lib.ssd_scan_get_status.argtypes = [vp, vp]
         lib.ssd_scan_get_status.restype = i32
+        lib.ssd_scan_gated_workspace_bytes.argtypes = [dims_p, i32, i64]
+        lib.ssd_scan_gated_workspace_bytes.restype = sz
+        lib.ssd_scan_fwd_gated.argtypes = [dims_p, vp, vp, fp, vp, vp, fp, fp, i32, vp, fp,
+                                           ctypes.c_float, i64, vp, fp, vp, sz, vp]
+        lib.ssd_scan_fwd_gated.restype = i32
         lib.ssd_scan_set_wait_cycles.argtypes = [ctypes.c_int64]
         lib.ssd_scan_set_wait_cycles.restype = ctypes.c_int64
         lib.ssd_scan_strerror.argtypes = [i32]
@@ -188,6 +193,52 @@ def ssd_scan_fwd(x, dt, A, B, C, D=None, initial_state=None, chunk_size: int = 2
     if rc != SSD_OK:
         raise SSDError(rc, "ssd_scan_fwd")
     return y, final_state
+
+
+def ssd_scan_gated_workspace_bytes(dims: ssd_dims, chunk_size: int, group_size: int) -> int:
+    return load_library().ssd_scan_gated_workspace_bytes(ctypes.byref(dims), int(chunk_size),
+                                                         int(group_size))
+
+
+def ssd_scan_fwd_gated(x, dt, A, B, C, z, D=None, initial_state=None, norm_weight=None,
+                       eps: float = 1e-5, group_size=None, chunk_size: int = 256, out=None,
+                       final_state=None, workspace=None, return_final_state: bool = True):
+    """out, final_state = gated_rmsnorm(scan(x, dt, A, B, C, D, initial_state), z).
+
+    out[..., f] = y / sqrt(mean over f's group of y^2 + eps) * norm_weight[f] * silu(z), with
+    f = h * P + p and groups of ``group_size`` consecutive features (default: one head,
+    ``P``).  Fused into the scan kernel where it can be (see include/ssd_scan.h).
+    """
+    _check_inputs(x, dt, A, B, C, D, initial_state)
+    if not x.is_cuda:
+        raise ValueError("ssd_scan_fwd_gated: tensors must be on a CUDA device")
+    if z.shape != x.shape or z.dtype != x.dtype or not z.is_contiguous():
+        raise ValueError("ssd_scan_fwd_gated: z must be shaped, typed and laid out like x")
+    b, L, H, P = x.shape
+    N = B.shape[3]
+    if norm_weight is not None and (norm_weight.shape != (H * P,)
+                                    or norm_weight.dtype != torch.float32
+                                    or not norm_weight.is_contiguous()):
+        raise ValueError("ssd_scan_fwd_gated: norm_weight must be contiguous float32 [H * P]")
+    g = P if group_size is None else int(group_size)
+    lib = load_library()
+    dims = make_dims(x, B)
+    if out is None:
+        out = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
+    need = lib.ssd_scan_gated_workspace_bytes(ctypes.byref(dims), int(chunk_size), g)
+    if need == 0:
+        raise SSDError(SSD_ERR_INVALID, "ssd_scan_gated_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    rc = lib.ssd_scan_fwd_gated(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                _ptr(D), _ptr(initial_state), int(chunk_size), _ptr(z),
+                                _ptr(norm_weight), float(eps), g, _ptr(out), _ptr(final_state),
+                                _ptr(workspace), workspace.numel(), _stream_handle(x.device))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_scan_fwd_gated")
+    return out, final_state
 
 
 def _cu_array(cu_seqlens):

@@ -32,6 +32,13 @@ struct ScanArgs {
     uint8_t* ws;               // workspace base (256-byte aligned)
     size_t ws_bytes;
     cudaStream_t stream;
+    // the gated RMSNorm fused into the output (tc128_launch with gated = 1 only): y receives
+    // rmsnorm(scan) * w * silu(z) over groups of `group` features
+    int gated = 0;
+    const void* z = nullptr;
+    const float* norm_w = nullptr;
+    float eps = 0.f;
+    int group = 0;
 };
 
 template <typename T> __device__ __forceinline__ float to_f32(T v);
@@ -109,6 +116,8 @@ int norm_launch(const NormArgs& a);
 // ssd_scan_set_wait_cycles).
 long long tc_wait_budget();
 int tc128_launch(const ScanArgs& a);
+// Whether the d_state 128 kernel fuses the gated RMSNorm for this headdim and group size.
+bool tc128_gated_supports(int64_t P, int group);
 size_t tc_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t P, int64_t N, int Q);
 bool tc_supports(int32_t dtype, int64_t P, int64_t N, int Q);
 int tc_launch(const ScanArgs& a);

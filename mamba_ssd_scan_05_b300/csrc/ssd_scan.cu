@@ -58,10 +58,18 @@ size_t workspace_for(const ssd_dims* d, int chunk_size, int resolved) {
                                    chunk_size);
 }
 
+// The gated RMSNorm to fuse into a tensor-core scan's output (ssd_scan_fwd_gated).
+struct Gate {
+    const void* z;
+    const float* w;
+    float eps;
+    int group;
+};
+
 int run(const ssd_dims* d, const void* x, const void* dt, const float* A, const void* B,
         const void* C, const float* D, const float* h0, int chunk_size, void* y, float* hT,
         void* workspace, size_t workspace_bytes, void* stream, int path,
-        bool clear_status = true) {
+        bool clear_status = true, const Gate* gate = nullptr) {
     const int r = resolve(d, chunk_size, path);
     if (r < 0) return -r;
     if (!A || (d->seqlen > 0 && (!x || !dt || !B || !C || !y))) return SSD_ERR_INVALID;
@@ -88,7 +96,25 @@ int run(const ssd_dims* d, const void* x, const void* dt, const float* A, const 
     a.dstate = d->dstate; a.ngroups = d->ngroups; a.dtype = d->dtype; a.chunk = chunk_size;
     a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.h0 = h0; a.y = y; a.hT = hT;
     a.ws = static_cast<uint8_t*>(workspace); a.ws_bytes = workspace_bytes; a.stream = st;
+    if (gate) {
+        a.gated = 1;
+        a.z = gate->z;
+        a.norm_w = gate->w;
+        a.eps = gate->eps;
+        a.group = gate->group;
+    }
     return r == SSD_PATH_TC ? tc_launch(a) : chunked_launch(a);
+}
+
+// Whether ssd_scan_fwd_gated fuses the norm into the scan kernel for this problem.
+bool gated_fused(const ssd_dims* d, int chunk_size, int64_t group) {
+    return resolve(d, chunk_size, SSD_PATH_AUTO) == SSD_PATH_TC && d->dstate == 128 &&
+           group <= 64 && tc128_gated_supports(d->headdim, (int)group);
+}
+
+// y scratch of the unfused form of ssd_scan_fwd_gated, after the scan's own workspace.
+size_t gated_scratch_offset(const ssd_dims* d, int chunk_size) {
+    return align_up(workspace_for(d, chunk_size, resolve(d, chunk_size, SSD_PATH_AUTO)), 256);
 }
 
 // Byte sizes of every tensor of a problem, in the host-arena order.
@@ -359,6 +385,48 @@ int ssd_gated_rmsnorm_fwd(int64_t rows, int64_t dim, int64_t group_size, int32_t
     return norm_launch(a);
 }
 
+size_t ssd_scan_gated_workspace_bytes(const ssd_dims* dims, int chunk_size, int64_t group_size) {
+    const int r = resolve(dims, chunk_size, SSD_PATH_AUTO);
+    if (r < 0 || group_size < 1 || (dims->nheads * dims->headdim) % group_size != 0) return 0;
+    if (gated_fused(dims, chunk_size, group_size)) return workspace_for(dims, chunk_size, r);
+    return gated_scratch_offset(dims, chunk_size) +
+           align_up(elem_bytes(dims->dtype) *
+                        (size_t)(dims->batch * dims->seqlen * dims->nheads * dims->headdim),
+                    256);
+}
+
+int ssd_scan_fwd_gated(const ssd_dims* dims, const void* x, const void* dt, const float* A,
+                       const void* B, const void* C, const float* D, const float* initial_state,
+                       int chunk_size, const void* z, const float* norm_weight, float eps,
+                       int64_t group_size, void* out, float* final_state, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    const int r = resolve(dims, chunk_size, SSD_PATH_AUTO);
+    if (r < 0) return -r;
+    const int64_t dim = dims->nheads * dims->headdim;
+    if (group_size < 1 || dim % group_size != 0) return SSD_ERR_INVALID;
+    if (!(eps >= 0.f) || eps > 1.0e30f) return SSD_ERR_INVALID;
+    if (dims->seqlen > 0 && (!z || !out)) return SSD_ERR_INVALID;
+    const bool fused = gated_fused(dims, chunk_size, group_size);
+    // z is read like y (16-byte vectors); the fused form reads the weight as float4
+    if (!aligned(z, 16) || !aligned(norm_weight, fused ? 16 : 4)) return SSD_ERR_INVALID;
+    if (!workspace || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
+    if (workspace_bytes < ssd_scan_gated_workspace_bytes(dims, chunk_size, group_size))
+        return SSD_ERR_WORKSPACE;
+    if (fused) {
+        const Gate g{z, norm_weight, eps, (int)group_size};
+        return run(dims, x, dt, A, B, C, D, initial_state, chunk_size, out, final_state,
+                   workspace, workspace_bytes, stream, SSD_PATH_AUTO, true, &g);
+    }
+    // unfused: the scan into the workspace's y scratch, then the gated RMSNorm kernel
+    const size_t off = gated_scratch_offset(dims, chunk_size);
+    void* ys = static_cast<uint8_t*>(workspace) + off;
+    int rc = run(dims, x, dt, A, B, C, D, initial_state, chunk_size, ys, final_state, workspace,
+                 off, stream, SSD_PATH_AUTO);
+    if (rc != SSD_OK) return rc;
+    return ssd_gated_rmsnorm_fwd(dims->batch * dims->seqlen, dim, group_size, dims->dtype, ys, z,
+                                 norm_weight, eps, out, stream);
+}
+
 int ssd_scan_get_status(void* workspace, void* stream) {
     if (!workspace) return SSD_ERR_INVALID;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -384,6 +452,6 @@ const char* ssd_scan_strerror(int code) {
     }
 }
 
-int ssd_scan_version(void) { return 200; }   // 0.2.0: + step, conv1d, gated RMSNorm, varlen
+int ssd_scan_version(void) { return 300; }   // 0.3.0: + fused gated scan, wait-limit setter
 
 }  // extern "C"

@@ -88,6 +88,9 @@ struct K3 {
     static constexpr uint32_t kOffSmall = kOffDt + kXSt * sizeof(DtSlot);
     static_assert(kOffDt % 16 == 0 && kOffSmall % 16 == 0, "16-byte aligned slots and barriers");
     static constexpr size_t kSmemBytes = kOffSmall + sizeof(Small) + 1024;   // + alignment slack
+    // the instance with the fused gated RMSNorm adds the row-sum exchange [128 rows][4] floats
+    static constexpr uint32_t kOffRed = (kOffSmall + sizeof(Small) + 15) / 16 * 16;
+    static constexpr size_t kSmemBytesGated = kOffRed + 128 * 4 * sizeof(float) + 1024;
     // TMEM columns
     static constexpr uint32_t kColG = 0;        // C B^T, fp32, 128 columns
     static constexpr uint32_t kColP = 128;      // P, bf16 pairs, 2 buffers x 64
@@ -97,7 +100,7 @@ struct K3 {
     static_assert(kColYoff + kPS <= kTmemCols, "TMEM budget");
     static_assert(kXSt <= kXStagesMax, "x ring");
     // at most 227 KB of dynamic shared memory per CTA on sm_103a
-    static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(kSmemBytes <= 232448 && kSmemBytesGated <= 232448, "shared memory");
 };
 
 // ------------------------------------------------------------------- producer roles ----------
@@ -310,7 +313,9 @@ __device__ __forceinline__ void ht_write_scaled(const float (&h)[CW], float s, u
 // A tile whose y epilogue is deferred to the next full tile.  Its x stage (the x row for the
 // D x term) and decay slot (the row factor, the mode) stay held until that epilogue has run.
 struct Pend {
-    __nv_bfloat16* row;     // y row at this thread's column block, or null past the sequence end
+    int64_t off;            // element offset of this thread's y (and z) row and column block,
+                            // or -1 past the sequence end
+    int64_t wcol;           // feature index of its first column (h * P + column)
     float d;                // D of the head
     int xs;                 // x / decay stage of the tile
 };
@@ -367,28 +372,100 @@ __device__ __forceinline__ P8 p_half_fallback(G16 g, int jb, int hf, int q, int 
     return o;
 }
 
-// y = s Y + D x for the 16 columns of this thread's row (s = the row factor on a factored tile,
-// 1 on a fallback tile, whose Y already holds Y_diag + e Y_off), rounded to bf16 and stored.
-__device__ __forceinline__ void store_y(__nv_bfloat16* row, float d, float sc, const float (&yv)[16],
-                                        const uint4 (&xv)[2]) {
+// silu(v) = v / (1 + exp(-v)) with the fast exponential and division (0 for v < -88).
+__device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.f + __expf(-v)); }
+
+// The output of this thread's 16 columns of a token row: y = s Y + D x (s = the row factor on
+// a factored tile, 1 on a fallback tile, whose Y already holds Y_diag + e Y_off).  Plain: y is
+// rounded to bf16 and stored.  Gated (kGated): out = y rsqrt(mean_group(y^2) + eps) w silu(z)
+// over groups of p.gsize consecutive features (Qiita "Mamba-2 / SSD" article, section 4.2,
+// step 4), from the float32 y; a group wider than the thread's 16 columns is summed across the
+// warps of the TMEM lane quarter through `red` (row sums) and red_bar[q] (bounded waits, two
+// phases: sums written, sums read).  Returns false on a timeout or abort.
+template <bool kGated>
+__device__ __forceinline__ bool emit(const Pend& pend, float sc, const float (&yv)[16],
+                                     const uint4 (&xv)[2], const TcParams& p, Small& sm,
+                                     float* red, int r, int wg, int q) {
+    float y[16];
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
         const uint32_t xin[4] = {xv[cc].x, xv[cc].y, xv[cc].z, xv[cc].w};
-        uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int i0 = cc * 8 + k * 2;
-            o[k] = pack_bf16x2(fmaf(d, bf16lo_to_f32(xin[k]), sc * yv[i0]),
-                               fmaf(d, bf16hi_to_f32(xin[k]), sc * yv[i0 + 1]));
+            y[i0] = fmaf(pend.d, bf16lo_to_f32(xin[k]), sc * yv[i0]);
+            y[i0 + 1] = fmaf(pend.d, bf16hi_to_f32(xin[k]), sc * yv[i0 + 1]);
         }
-        if (row) *reinterpret_cast<uint4*>(row + cc * 8) = make_uint4(o[0], o[1], o[2], o[3]);
     }
+    if constexpr (kGated) {
+        uint4 zv[2] = {};
+        if (pend.off >= 0) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc)
+                zv[cc] = *reinterpret_cast<const uint4*>(p.z + pend.off + cc * 8);
+        }
+        float s0 = 0.f, s1 = 0.f;     // sums of squares of columns 0-7 and 8-15
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            s0 = fmaf(y[i], y[i], s0);
+            s1 = fmaf(y[8 + i], y[8 + i], s1);
+        }
+        float ss0 = s0, ss1 = s1;     // the sums over each column's group
+        if (p.gsize >= 16) ss0 = ss1 = s0 + s1;
+        if (p.gsize > 16) {
+            red[r * 4 + wg] = ss0;
+            mbar_arrive(&sm.red_bar[q]);
+            if (!wait_warp(&sm.red_bar[q], 0u, sm, p)) return false;
+            const float* rr = red + r * 4;
+            ss0 = ss1 = p.gsize == 32 ? rr[wg & 2] + rr[(wg & 2) + 1] : (rr[0] + rr[1]) + (rr[2] + rr[3]);
+            mbar_arrive(&sm.red_bar[q]);
+            if (!wait_warp(&sm.red_bar[q], 1u, sm, p)) return false;
+        }
+        const float inv = 1.f / (float)p.gsize;
+        const float rs0 = rsqrtf(fmaf(ss0, inv, p.eps)), rs1 = rsqrtf(fmaf(ss1, inv, p.eps));
+        float wv[16];
+        if (p.nw) {
+            const float4* wp = reinterpret_cast<const float4*>(p.nw + pend.wcol);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 f = wp[i];
+                wv[4 * i] = f.x; wv[4 * i + 1] = f.y; wv[4 * i + 2] = f.z; wv[4 * i + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) wv[i] = 1.f;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const uint32_t zin[4] = {zv[cc].x, zv[cc].y, zv[cc].z, zv[cc].w};
+            const float rsc = cc ? rs1 : rs0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i0 = cc * 8 + k * 2;
+                y[i0] *= rsc * wv[i0] * silu_fast(bf16lo_to_f32(zin[k]));
+                y[i0 + 1] *= rsc * wv[i0 + 1] * silu_fast(bf16hi_to_f32(zin[k]));
+            }
+        }
+    }
+    if (pend.off >= 0) {
+        __nv_bfloat16* row = p.y + pend.off;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+            *reinterpret_cast<uint4*>(row + cc * 8) =
+                make_uint4(pack_bf16x2(y[cc * 8 + 0], y[cc * 8 + 1]),
+                           pack_bf16x2(y[cc * 8 + 2], y[cc * 8 + 3]),
+                           pack_bf16x2(y[cc * 8 + 4], y[cc * 8 + 5]),
+                           pack_bf16x2(y[cc * 8 + 6], y[cc * 8 + 7]));
+    }
+    return true;
 }
 
 // The last pending epilogue of the CTA (after its loop).
+template <bool kGated>
 __device__ __forceinline__ bool last_epilogue(Pend pend, int pj, Small* sm, const TcParams* p,
-                                           const DtSlot* slots, const uint8_t* smem,
-                                           uint32_t tmem, uint32_t lane_base, int r, int wg) {
+                                              const DtSlot* slots, const uint8_t* smem,
+                                              float* red, uint32_t tmem, uint32_t lane_base,
+                                              int r, int wg, int q) {
     const int yb = pj & 1;
     const DtSlot& ps = slots[pend.xs];
     const float e = ps.e[r];
@@ -411,8 +488,7 @@ __device__ __forceinline__ bool last_epilogue(Pend pend, int pj, Small* sm, cons
     mbar_arrive(&sm->y_empty[yb]);
     if (!fac) mbar_arrive(&sm->yoff_empty);
     mbar_arrive(&sm->x_empty[pend.xs]);
-    store_y(pend.row, pend.d, fac ? e : 1.f, yv, xv);
-    return true;
+    return emit<kGated>(pend, fac ? e : 1.f, yv, xv, *p, *sm, red, r, wg, q);
 }
 
 // bf16 (s h)^T into the MN-major, 128-byte swizzled h^T tile (128 rows x 64 columns): the B
@@ -431,6 +507,7 @@ __device__ __forceinline__ void ht_write_scaled(const float (&h)[16], float s, u
 // Warps 4-19: compute warpgroup wg (headdim columns c0 = 16 wg ..), lane quarter q (TMEM lanes,
 // tile rows and state rows 32q .. 32q+31).  Per tile: the scaled x tile, this tile's P block,
 // the previous tile's y, the state.  Returns false on a timeout or abort.
+template <bool kGated>
 __device__ __forceinline__ bool role_compute(const Plan& plan, Small& sm, const TcParams& p,
                                              uint8_t* smem, const DtSlot* slots, uint32_t tmem,
                                              int w, int lane) {
@@ -442,6 +519,7 @@ __device__ __forceinline__ bool role_compute(const Plan& plan, Small& sm, const 
     const int r = q * 32 + lane;             // tile row, and state row
     const int c0 = wg * CW;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    float* red = reinterpret_cast<float*>(smem + K::kOffRed);   // gated instance only
     float h[CW];
     Pend pend{};
     bool have_pend = false;
@@ -516,6 +594,7 @@ __device__ __forceinline__ bool role_compute(const Plan& plan, Small& sm, const 
                 float g0[16], g1[16];
                 const uint32_t tg = tmem + lane_base + K::kColG + 32 * wg;
                 tmem_ld16x2(tg, g0, tg + 16, g1);
+                SSD_TC_TRACE_POINT(22, nt);
                 const uint32_t tp = tmem + lane_base + K::kColP + pb * kPS + 16 * wg;
                 uint32_t pk[8];
                 if (sl.fac) {
@@ -565,6 +644,7 @@ __device__ __forceinline__ bool role_compute(const Plan& plan, Small& sm, const 
                 for (int cc = 0; cc < 2; ++cc)
                     xv[cc] = *reinterpret_cast<const uint4*>(xrow + sw128_off(r, wg * 2 + cc));
                 if (!wait_warp(&sm.y_full[pyb], (uint32_t)((j - 1) >> 1) & 1u, sm, p)) return false;
+                SSD_TC_TRACE_POINT(40, nt);
                 tc_fence_after();
                 float yv[16];
                 if (pfac) {
@@ -576,11 +656,13 @@ __device__ __forceinline__ bool role_compute(const Plan& plan, Small& sm, const 
 #pragma unroll
                     for (int i = 0; i < 16; ++i) yv[i] = fmaf(pe, yo[i], yv[i]);
                 }
+                SSD_TC_TRACE_POINT(42, nt);
                 tc_fence_before();
                 mbar_arrive(&sm.y_empty[pyb]);
                 if (!pfac) mbar_arrive(&sm.yoff_empty);
                 mbar_arrive(&sm.x_empty[pend.xs]);
-                store_y(pend.row, pend.d, pfac ? pe : 1.f, yv, xv);
+                if (!emit<kGated>(pend, pfac ? pe : 1.f, yv, xv, p, sm, red, r, wg, q))
+                    return false;
                 have_pend = false;
             }
             SSD_TC_TRACE_POINT(41, nt);
@@ -599,6 +681,7 @@ __device__ __forceinline__ bool role_compute(const Plan& plan, Small& sm, const 
         {
             float sv[CW];
             tmem_ld16(tmem + lane_base + K::kColS + c0, sv);
+            SSD_TC_TRACE_POINT(34, nt);
 #pragma unroll
             for (int i = 0; i < CW; ++i) h[i] = fmaf(decay, h[i], sigma * sv[i]);
         }
@@ -620,9 +703,8 @@ __device__ __forceinline__ bool role_compute(const Plan& plan, Small& sm, const 
         // a state-only tile releases its stage now
         if (full_tile) {
             const int64_t t = (int64_t)c.k * kTile + r;
-            pend.row = t < p.L ? p.y + (((int64_t)uc.b * p.L + t) * p.H + uc.h) * p.P +
-                                     uc.ps * kPS + c0
-                               : nullptr;
+            pend.wcol = (int64_t)uc.h * p.P + uc.ps * kPS + c0;
+            pend.off = t < p.L ? ((int64_t)uc.b * p.L + t) * p.H * p.P + pend.wcol : -1;
             pend.d = Dh;
             pend.xs = xs;
             have_pend = true;
@@ -640,13 +722,15 @@ __device__ __forceinline__ bool role_compute(const Plan& plan, Small& sm, const 
             item_exit_state(hs, &p, c.it.fin, uc.bh, uc.ps, w, lane, r, c0, item_logd);
         }
     }
-    if (have_pend && !last_epilogue(pend, j - 1, &sm, &p, slots, smem, tmem, lane_base, r, wg))
+    if (have_pend &&
+        !last_epilogue<kGated>(pend, j - 1, &sm, &p, slots, smem, red, tmem, lane_base, r, wg, q))
         return false;
     return true;
 }
 
 // ------------------------------------------------------------------- the kernel --------------
 
+template <bool kGated>
 __global__ void __launch_bounds__(K3::kThreads, 1)
     ssd_tc128_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmB,
@@ -683,6 +767,7 @@ __global__ void __launch_bounds__(K3::kThreads, 1)
         mbar_init(&sm.h_full, kC);
         mbar_init(&sm.h_empty, 1);
         mbar_init(&sm.yoff_empty, kC);
+        for (int i = 0; i < 4; ++i) mbar_init(&sm.red_bar[i], 128);
         mbar_init(&sm.mma_done, 1);
         sm.abort_flag = 0;
         sm.plan = plan::make_plan(p.n_units, p.n_tiles, p.n_ctas, p.pass1_mode, blockIdx.x);
@@ -742,7 +827,7 @@ __global__ void __launch_bounds__(K3::kThreads, 1)
         }
     } else {
         regs_inc<K::kRegsCompute>();
-        role_compute(plan, sm, p, smem, slots, tmem, warp - kWarpC, lane);
+        role_compute<kGated>(plan, sm, p, smem, slots, tmem, warp - kWarpC, lane);
     }
 
     // single-lane roles (B / C TMA) reconverge their warp before the CTA barrier
@@ -755,15 +840,20 @@ __global__ void __launch_bounds__(K3::kThreads, 1)
 
 }  // namespace
 
-int tc128_launch(const ScanArgs& a) {
+namespace {
+
+template <bool kGated>
+int launch128(const ScanArgs& a, const TcParams& p) {
     using K = K3;
+    constexpr size_t smem = kGated ? K::kSmemBytesGated : K::kSmemBytes;
     // the setmaxnreg split must fit in the registers the kernel is launched with: check what
     // the compiler gave it before the first launch (a split that does not fit would never
     // complete)
     static int regs_ok = -1;
     if (regs_ok < 0) {
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, ssd_tc128_kernel) != cudaSuccess) return SSD_ERR_CUDA;
+        if (cudaFuncGetAttributes(&fa, ssd_tc128_kernel<kGated>) != cudaSuccess)
+            return SSD_ERR_CUDA;
         regs_ok = (fa.numRegs == K::kRegsLaunch && fa.maxThreadsPerBlock >= K::kThreads) ? 1 : 0;
     }
     if (!regs_ok) return SSD_ERR_UNSUPPORTED;
@@ -772,6 +862,24 @@ int tc128_launch(const ScanArgs& a) {
         !make_map(&tmB, a.B, a.dstate, a.ngroups, a.seqlen, a.batch) ||
         !make_map(&tmC, a.C, a.dstate, a.ngroups, a.seqlen, a.batch))
         return SSD_ERR_CUDA;
+    if (cudaMemsetAsync(p.flags, 0, sizeof(int) * kFlagsPerCta * (size_t)p.n_ctas, a.stream) !=
+        cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (cudaFuncSetAttribute(ssd_tc128_kernel<kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    ssd_tc128_kernel<kGated><<<(unsigned)p.n_ctas, K::kThreads, smem, a.stream>>>(tmX, tmB, tmC, p);
+    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // namespace
+
+bool tc128_gated_supports(int64_t P, int group) {
+    return P % kPS == 0 && (group == 8 || group == 16 || group == 32 || group == 64);
+}
+
+int tc128_launch(const ScanArgs& a) {
+    if (a.gated && !tc128_gated_supports(a.headdim, a.group)) return SSD_ERR_UNSUPPORTED;
     const int nsm = sm_count();
     if (nsm <= 0) return SSD_ERR_CUDA;
     TcParams p;
@@ -793,15 +901,11 @@ int tc128_launch(const ScanArgs& a) {
     p.flags = reinterpret_cast<int*>(a.ws + kWsHeaderBytes);
     p.slots = reinterpret_cast<float*>(a.ws + kWsHeaderBytes + flags_bytes());
     p.budget = tc_wait_budget();
-    if (cudaMemsetAsync(p.flags, 0, sizeof(int) * kFlagsPerCta * (size_t)p.n_ctas, a.stream) !=
-        cudaSuccess)
-        return SSD_ERR_CUDA;
-    if (cudaFuncSetAttribute(ssd_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)K::kSmemBytes) != cudaSuccess)
-        return SSD_ERR_CUDA;
-    ssd_tc128_kernel<<<(unsigned)p.n_ctas, K::kThreads, K::kSmemBytes, a.stream>>>(tmX, tmB, tmC,
-                                                                                  p);
-    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    p.z = static_cast<const __nv_bfloat16*>(a.z);
+    p.nw = a.norm_w;
+    p.eps = a.eps;
+    p.gsize = a.group;
+    return a.gated ? launch128<true>(a, p) : launch128<false>(a, p);
 }
 
 }  // namespace ssd

@@ -83,6 +83,12 @@ struct TcParams {
     int* flags;         // per CTA and compute warp: inclusive flag, aggregate flag, log2 decay
     float* slots;       // per CTA: inclusive state [64 x N], then aggregate state [64 x N]
     long long budget;   // clock64 cycles a single wait may take
+    // the gated RMSNorm applied in the epilogue (the kernel instance that fuses it): z as y,
+    // the norm weight [H * P] (or null), eps, and the group size (8, 16, 32 or 64 features)
+    const __nv_bfloat16* z;
+    const float* nw;
+    float eps;
+    int gsize;
 };
 
 struct Small {
@@ -94,6 +100,7 @@ struct Small {
     uint64_t y_full[2], y_empty[2];
     uint64_t pb_empty[2];           // P buffer free (double-buffered P)
     uint64_t yoff_empty;            // separate off-diagonal accumulator free (fallback tiles)
+    uint64_t red_bar[4];            // per TMEM lane quarter: the fused norm's row sums exchanged
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
