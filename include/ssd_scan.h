@@ -243,12 +243,15 @@ int ssd_step_fwd(const ssd_dims* dims,
  *   - state_in:     [batch, width - 1, channels] T, or NULL: the width - 1 inputs before x
  *   - state_out:    [batch, width - 1, channels] T, or NULL (not written): the last width - 1
  *                   inputs of state_in ++ x, so the next call continues the sequence
- *   - 1 <= width <= 8, batch <= 65535, seqlen <= 1048560 (65535 blocks of 16 tokens; longer
- *     sequences: SSD_ERR_UNSUPPORTED, or split them and carry the state).  Element alignment suffices;
- *     16-byte aligned buffers with channels % (16 / sizeof(T)) == 0 take the vector path.
+ *   - 1 <= width <= 8, batch <= 65535.  Element alignment suffices.  16-byte aligned x, out
+ *     and states with channels % (16 / sizeof(T)) == 0 take the streaming kernel (tiles of 64
+ *     tokens through shared memory by TMA; seqlen < 2^31 - 2^16); other buffers the register
+ *     kernel (seqlen <= 1048560 = 65535 blocks of 16 tokens, else SSD_ERR_UNSUPPORTED: split
+ *     the sequence and carry the state).
  *   - No output may overlap an input, and state_out may not overlap out (SSD_ERR_INVALID).
  *   - Needs no workspace; enqueued on `stream`.  Returns SSD_OK, SSD_ERR_INVALID,
- *     SSD_ERR_UNSUPPORTED (sizes beyond the grid limits) or SSD_ERR_CUDA.
+ *     SSD_ERR_UNSUPPORTED (sizes beyond the grid limits) or SSD_ERR_CUDA.  A bounded device
+ *     wait of the streaming kernel that gives up is reported by ssd_block_get_status.
  */
 int ssd_causal_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t channels, int width,
                           int32_t dtype, const void* x, const float* weight, const float* bias,
@@ -265,15 +268,27 @@ int ssd_causal_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t channels, int w
  *   - z NULL: no gate.  weight: [dim] float32, or NULL (ones).  eps >= 0 (the pages give no
  *     value; 1e-5 is the binding's default).  group_size divides dim (dim: one group per row).
  *   - dim / group_size <= 12288, rows <= 2^31 - 1 (else SSD_ERR_UNSUPPORTED).
- *   - out may equal y or z (each element is read before it is written by the same thread);
- *     element alignment suffices, 16-byte alignment with group_size % (16 / sizeof(T)) == 0
- *     takes the vector path.
+ *   - out may equal y or z (a row is read completely before any of it is written); element
+ *     alignment suffices.  16-byte aligned buffers with group_size % (16 / sizeof(T)) == 0 and
+ *     rows of y (and z) up to 48 KB take the streaming kernel (whole rows through shared memory
+ *     by bulk copies); others the register kernel.
  *   - Needs no workspace; enqueued on `stream`.  Returns SSD_OK, SSD_ERR_INVALID,
- *     SSD_ERR_UNSUPPORTED or SSD_ERR_CUDA.
+ *     SSD_ERR_UNSUPPORTED or SSD_ERR_CUDA.  A bounded device wait of the streaming kernel that
+ *     gives up is reported by ssd_block_get_status.
  */
 int ssd_gated_rmsnorm_fwd(int64_t rows, int64_t dim, int64_t group_size, int32_t dtype,
                           const void* y, const void* z, const float* weight, float eps,
                           void* out, void* stream);
+
+/*
+ * ssd_block_get_status -- the device-side status of the streaming conv1d and RMSNorm kernels
+ * (which take no workspace): synchronises `stream`, then returns SSD_OK, or SSD_ERR_TIMEOUT if
+ * a bounded wait of one of those kernels gave up (ssd_scan_set_wait_cycles sets the limit; the
+ * kernel then stops early and its output is incomplete) since the last call, and clears it.
+ * The word is per device and shared by all streams of the process.  SSD_ERR_CUDA if the
+ * synchronisation or the read failed.
+ */
+int ssd_block_get_status(void* stream);
 
 /*
  * ssd_scan_fwd_gated -- the scan followed by the gated RMSNorm of its output, the block's next
@@ -310,9 +325,10 @@ int ssd_scan_fwd_gated(const ssd_dims* dims,
 int ssd_scan_get_status(void* workspace, void* stream);
 
 /* Limit, in SM clock cycles, of every device-side wait of the tensor-core kernels (a barrier
- * between warp roles, or the hand-off of a running state between thread blocks).  A wait that
- * reaches it makes the kernel stop, record SSD_ERR_TIMEOUT in the workspace status word
- * (ssd_scan_get_status) and return; the context stays usable.  cycles <= 0 restores the
+ * between warp roles, or the hand-off of a running state between thread blocks) and of the
+ * streaming conv1d / RMSNorm kernels (a copy into shared memory).  A wait that reaches it makes
+ * the kernel stop, record SSD_ERR_TIMEOUT in the workspace status word (ssd_scan_get_status;
+ * ssd_block_get_status for the conv1d and RMSNorm) and return; the context stays usable.  cycles <= 0 restores the
  * default, 2^32 cycles (about 2 s at the B300's maximum SM clock).  The setting is process-wide
  * and applies to launches enqueued after the call; a limit far below a wait's normal length
  * makes calls fail with SSD_ERR_TIMEOUT, which is what tests of the timeout path use it for.

@@ -30,6 +30,7 @@ from ._binding import (  # noqa: F401
     ssd_scan_host_arena_bytes,
     ssd_scan_resolve_path,
     ssd_scan_set_wait_cycles,
+    ssd_block_get_status,
     ssd_scan_strerror,
     ssd_scan_varlen_workspace_bytes,
     ssd_scan_version,

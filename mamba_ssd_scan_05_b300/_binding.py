@@ -86,6 +86,8 @@ def load_library(path: str = LIB_PATH):
                                            ctypes.c_float, i64, vp, fp, vp, sz, vp]
         lib.ssd_scan_fwd_gated.restype = i32
         lib.ssd_scan_set_wait_cycles.argtypes = [ctypes.c_int64]
+        lib.ssd_block_get_status.argtypes = [ctypes.c_void_p]
+        lib.ssd_block_get_status.restype = i32
         lib.ssd_scan_set_wait_cycles.restype = ctypes.c_int64
         lib.ssd_scan_strerror.argtypes = [i32]
         lib.ssd_scan_strerror.restype = ctypes.c_char_p
@@ -385,6 +387,14 @@ def ssd_scan_get_status(workspace, device=None) -> int:
     """Synchronise the current stream and return (and clear) the workspace status word."""
     lib = load_library()
     return lib.ssd_scan_get_status(_ptr(workspace), _stream_handle(device or workspace.device))
+
+
+def ssd_block_get_status(device=None) -> int:
+    """Synchronise the current stream of ``device`` and return (and clear) the status word of the
+    streaming conv1d / RMSNorm kernels (SSD_OK, or SSD_ERR_TIMEOUT after a wait gave up)."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    return lib.ssd_block_get_status(_stream_handle(dev))
 
 
 def ssd_scan_set_wait_cycles(cycles: int) -> int:

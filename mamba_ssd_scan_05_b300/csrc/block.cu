@@ -14,14 +14,15 @@
 // Both read every input element once and write every output element once; the layouts are
 // channel-last (the scan's own [batch, seqlen, heads * headdim]), so a thread moves 16-byte
 // vectors of consecutive channels and a warp 512 contiguous bytes.
+#include "block_math.cuh"
 #include "common.cuh"
 
 namespace ssd {
 namespace {
 
-// silu(v) = v / (1 + exp(-v)), with the fast exponential and division: each within a few ulp
-// over the range that matters; for v < -88 the denominator overflows and the result is 0.
-__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.f + __expf(-v)); }
+// silu(v) = v / (1 + exp(-v)): the shared form of block_math.cuh (the streaming kernels of
+// block_staged.cu compute the same bits)
+__device__ __forceinline__ float silu_f(float v) { return bm::silu1(v); }
 
 // VEC consecutive elements of T <-> float, at a 16-byte aligned address when VEC > 1.
 template <typename T, int VEC> struct Vec;
@@ -345,6 +346,9 @@ int norm_launch_t(const NormArgs& a, const NormParams& p) {
 }  // namespace
 
 int norm_launch(const NormArgs& a) {
+    // the streaming kernel (block_staged.cu) for aligned rows that fit two ring stages
+    const int st = norm_staged_launch(a);
+    if (st != SSD_ERR_UNSUPPORTED) return st;
     NormParams p;
     p.D = a.dim; p.g = a.group_size; p.y = a.y; p.z = a.z; p.w = a.weight; p.eps = a.eps;
     p.out = a.out;
@@ -357,6 +361,9 @@ int norm_launch(const NormArgs& a) {
 }
 
 int conv_launch(const ConvArgs& a) {
+    // the streaming kernel (block_staged.cu) for 16-byte aligned rows of channels
+    const int st = conv_staged_launch(a);
+    if (st != SSD_ERR_UNSUPPORTED) return st;
     ConvParams p;
     p.L = a.seqlen; p.C = a.channels; p.x = a.x; p.w = a.weight; p.bias = a.bias;
     p.s_in = a.s_in; p.s_out = a.s_out; p.out = a.out; p.silu = a.silu;

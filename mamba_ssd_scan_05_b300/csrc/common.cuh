@@ -97,6 +97,9 @@ struct ConvArgs {
     cudaStream_t stream;
 };
 int conv_launch(const ConvArgs& a);
+// The shared-memory streaming form (block_staged.cu); SSD_ERR_UNSUPPORTED where it does not
+// apply (nothing launched).
+int conv_staged_launch(const ConvArgs& a);
 
 // Gated RMSNorm (block.cu), after validation.
 struct NormArgs {
@@ -110,6 +113,7 @@ struct NormArgs {
     cudaStream_t stream;
 };
 int norm_launch(const NormArgs& a);
+int norm_staged_launch(const NormArgs& a);
 
 // Tensor-core path (tc.cu; the d_state 128 kernel in tc128.cu).
 // Cycles a single device-side wait of the tensor-core kernels may take (process-wide setting,

@@ -6,8 +6,8 @@ import torch
 
 import oracle
 from oracle import block
-from mamba_ssd_scan_05_b300 import (SSDError, ssd_causal_conv1d_fwd, ssd_gated_rmsnorm_fwd,
-                                    workloads)
+from mamba_ssd_scan_05_b300 import (SSDError, ssd_block_get_status, ssd_causal_conv1d_fwd,
+                                    ssd_gated_rmsnorm_fwd, ssd_scan_set_wait_cycles, workloads)
 
 pytestmark = pytest.mark.gpu
 
@@ -45,6 +45,13 @@ CONV = [
     # several 64-token blocks with a ragged end; 96- and 128-thread blocks over the channels
     (1, 300, 768, 4, "bf16", True, True, True),
     (2, 129, 1024, 4, "f32", False, True, True),
+    # streaming kernel: channel tails inside a 256-byte tile column, token tails, every width
+    (2, 200, 200, 4, "bf16", True, True, True),
+    (1, 1000, 1000, 4, "f32", True, True, True),
+    (3, 64, 136, 8, "bf16", True, True, True),
+    (1, 65, 520, 2, "bf16", False, True, True),
+    (2, 130, 8, 6, "bf16", True, False, True),
+    (1, 3, 4, 5, "f32", True, True, True),
 ]
 
 
@@ -64,6 +71,32 @@ def test_conv_matches_oracle(case):
     # the new state is the last K - 1 inputs: exact copies
     if K > 1:
         assert np.array_equal(st.float().cpu().double().numpy(), ref_st), f"{case} state"
+
+
+def _misaligned(t):
+    """A copy of t whose data starts one element past a 16-byte boundary (the register kernel
+    then runs instead of the streaming one)."""
+    flat = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    v = flat[1:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("K", [1, 4, 8])
+def test_conv_streaming_and_register_kernels_agree_bitwise(dt, K):
+    """Both kernels evaluate bias + sum_k w x in the same order and the same SiLU, so the two
+    outputs and states must be equal bit for bit."""
+    inp = cuda(workloads.make_conv_inputs(2, 333, 264, K, dt, seed=K, state=True))
+    out, st = ssd_causal_conv1d_fwd(inp["x"], inp["weight"], inp["bias"], inp["state"],
+                                    return_state=True)
+    xm = _misaligned(inp["x"])
+    sm = _misaligned(inp["state"]) if K > 1 else None
+    out2, st2 = ssd_causal_conv1d_fwd(xm, inp["weight"], inp["bias"], sm, return_state=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+    if K > 1:
+        assert torch.equal(st, st2)
 
 
 def test_conv_split_sequence_equals_one_call_bitwise():
@@ -165,6 +198,51 @@ def test_norm_workload_full_size_sampled_rows():
     ref = block.gated_rmsnorm(inp["y"][rows], inp["z"][rows], inp["weight"], 1e-5,
                               n["group_size"])
     close(out[rows].float().cpu(), ref, n["dtype"], "norm workload")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_norm_streaming_and_register_kernels_both_match_oracle(dt):
+    """The same rows through the streaming kernel (aligned) and the register kernel (one
+    element off a 16-byte boundary); several groups per row, more rows than the grid holds."""
+    inp = workloads.make_norm_inputs(3000, 768, dt, seed=77)
+    dev = cuda(inp)
+    ref = block.gated_rmsnorm(inp["y"], inp["z"], inp["weight"], 1e-5, 64)
+    a = ssd_gated_rmsnorm_fwd(dev["y"], dev["z"], dev["weight"], group_size=64)
+    b = ssd_gated_rmsnorm_fwd(_misaligned(dev["y"]), _misaligned(dev["z"]), dev["weight"],
+                              group_size=64)
+    torch.cuda.synchronize()
+    close(a.float().cpu(), ref, dt, "streaming")
+    close(b.float().cpu(), ref, dt, "register")
+
+
+def test_block_kernels_wait_limit_runs_out_then_next_call_is_clean():
+    """With a wait limit of one cycle, any wait of the streaming kernels that is not satisfied
+    at its first poll gives up (over thousands of HBM-bound tiles some always are): the kernels
+    stop and report SSD_ERR_TIMEOUT through ssd_block_get_status.  With the default limit the
+    next calls match the oracle and report SSD_OK."""
+    cin = workloads.make_conv_inputs(4, 2048, 2048, 4, "bf16", seed=5)
+    nin = workloads.make_norm_inputs(8192, 2048, "bf16", seed=6)
+    cd, nd = cuda(cin), cuda(nin)
+    assert ssd_block_get_status() == 0
+    for run in ("conv", "norm"):
+        ssd_scan_set_wait_cycles(1)
+        try:
+            if run == "conv":
+                ssd_causal_conv1d_fwd(cd["x"], cd["weight"], cd["bias"])
+            else:
+                ssd_gated_rmsnorm_fwd(nd["y"], nd["z"], nd["weight"])
+            status = ssd_block_get_status()
+        finally:
+            ssd_scan_set_wait_cycles(0)
+        assert status == 4, f"{run}: expected SSD_ERR_TIMEOUT, got {status}"
+        assert ssd_block_get_status() == 0, "the status word is cleared by the read"
+    out = ssd_causal_conv1d_fwd(cd["x"], cd["weight"], cd["bias"])
+    nout = ssd_gated_rmsnorm_fwd(nd["y"], nd["z"], nd["weight"])
+    assert ssd_block_get_status() == 0
+    ref, _ = block.causal_conv1d(cin["x"], cin["weight"], cin["bias"], None)
+    close(out.float().cpu(), ref, "bf16", "conv after timeout")
+    close(nout.float().cpu(), block.gated_rmsnorm(nin["y"], nin["z"], nin["weight"]), "bf16",
+          "norm after timeout")
 
 
 def test_norm_rejects_bad_groups():
