@@ -53,9 +53,9 @@ __device__ __forceinline__ void st_flag_abort(StCtl* ctl) {
 // Bounded wait of one thread for a ring stage.  False if it gave up (this thread's timeout,
 // which raises the CTA's abort flag, or another thread's abort flag).  The CTA decides to stop
 // with __syncthreads_or over these results, so that every thread leaves the loop together.
-// A poll suspends the thread for at most hint_ns, a quarter of the budget in nanoseconds at
-// 1 GHz or more; budgets too short for the hardware's suspension granularity (spin) poll
-// without suspending, so that no poll outlasts the budget.
+// A poll suspends the thread for at most hint_ns (wait_hint); budgets too short for the
+// hardware's suspension granularity (spin) poll without suspending, so that no poll outlasts
+// the budget.
 __device__ __forceinline__ bool st_poll(uint64_t* bar, uint32_t parity, uint32_t hint_ns,
                                         bool spin) {
     return spin ? mbar_test_wait(bar, parity) : mbar_try_wait_ns(bar, parity, hint_ns);
@@ -475,7 +475,7 @@ constexpr size_t kStMaxSmem = 200u << 10;
 constexpr long long kSpinBudget = 1 << 16;   // budgets up to this many cycles poll without suspending
 
 // budget / 4 nanoseconds (at most 1 ms, at least 1): below the budget at any SM clock >= 1 GHz
-uint32_t hint_for(long long budget) {
+uint32_t wait_hint(long long budget) {
     return (uint32_t)std::max<long long>(1, std::min<long long>(budget / 4, 1000000));
 }
 
@@ -504,7 +504,7 @@ int norm_staged_v(const NormArgs& a, int threads) {
     // up to 64 KB of rows in flight per CTA (two or more CTAs per SM), at least two stages
     p.stages = (int)std::min<size_t>(kStMaxStages, std::max<size_t>(2, (64u << 10) / stage));
     p.budget = tc_wait_budget();
-    p.hint_ns = hint_for(p.budget);
+    p.hint_ns = wait_hint(p.budget);
     p.spin = p.budget <= kSpinBudget;
     const size_t smem =
         kStCtlBytes + p.stages * stage + 3 * sizeof(float) * (size_t)(a.dim / a.group_size);
@@ -563,7 +563,7 @@ int conv_staged_k(const ConvArgs& a) {
     p.rows = p.ntt * a.batch;
     p.w = a.weight; p.bias = a.bias; p.s_in = a.s_in; p.s_out = a.s_out; p.out = a.out;
     p.budget = tc_wait_budget();
-    p.hint_ns = hint_for(p.budget);
+    p.hint_ns = wait_hint(p.budget);
     p.spin = p.budget <= kSpinBudget;
     if (p.rows == 0) return SSD_OK;
     CUtensorMap tmx, tmo;
