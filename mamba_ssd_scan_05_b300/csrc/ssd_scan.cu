@@ -3,6 +3,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -133,6 +134,44 @@ Sizes sizes_of(const ssd_dims* d) {
     return s;
 }
 
+// ---- the host-buffer entry point's copy pipeline ----------------------------------------------
+
+constexpr int kHostPieces = 8;          // at most this many pieces per call
+
+// Per device: a copy-in and a copy-out stream and the events that order them against the
+// caller's stream, created on first use and kept for the life of the process.  Calls enqueue
+// under the mutex, so an event is never re-recorded before the previous call's waits on it
+// have been enqueued.
+struct HostPipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t in_done[kHostPieces] = {}, scan_done[kHostPieces] = {};
+    bool ready = false;
+};
+std::mutex g_pipe_mutex;
+HostPipe g_pipe[64];
+
+int host_pipe(HostPipe** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SSD_ERR_CUDA;
+    HostPipe& hp = g_pipe[dev];
+    if (!hp.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        if (cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.fork, ef) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.join, ef) != cudaSuccess)
+            return SSD_ERR_CUDA;
+        for (int i = 0; i < kHostPieces; ++i)
+            if (cudaEventCreateWithFlags(&hp.in_done[i], ef) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.scan_done[i], ef) != cudaSuccess)
+                return SSD_ERR_CUDA;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return SSD_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -198,22 +237,99 @@ int ssd_scan_fwd_host(const ssd_dims* dims, const void* x, const void* dt, const
     const size_t ws_bytes = arena_bytes - (size_t)(p - static_cast<uint8_t*>(device_arena));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
-    if ((s.x && cudaMemcpyAsync(dx, x, s.x, h2d, st) != cudaSuccess) ||
-        (s.dt && cudaMemcpyAsync(ddt, dt, s.dt, h2d, st) != cudaSuccess) ||
-        cudaMemcpyAsync(dA, A, s.A, h2d, st) != cudaSuccess ||
-        (s.bc && cudaMemcpyAsync(dB, B, s.bc, h2d, st) != cudaSuccess) ||
-        (s.bc && cudaMemcpyAsync(dC, C, s.bc, h2d, st) != cudaSuccess) ||
-        (D && cudaMemcpyAsync(dD, D, s.D, h2d, st) != cudaSuccess) ||
-        (initial_state && cudaMemcpyAsync(dh0, initial_state, s.st, h2d, st) != cudaSuccess))
-        return SSD_ERR_CUDA;
-    const int rc = run(dims, dx, ddt, dA, dB, dC, D ? dD : nullptr,
-                       initial_state ? dh0 : nullptr, chunk_size, dy,
-                       final_state ? dhT : nullptr, dws, ws_bytes, stream, SSD_PATH_AUTO);
+
+    // Pieces: groups of batch rows (independent problems) when there are several rows, else
+    // stretches of the sequence whose state is carried on the device (multiples of 256 tokens,
+    // so each piece boundary is also a chunk and tile boundary).  Piece p's copies in run on
+    // the copy-in stream while piece p - 1 scans on `stream` and piece p - 2's outputs go back
+    // on the copy-out stream.
+    const int64_t b = dims->batch, L = dims->seqlen;
+    const bool by_rows = b > 1;
+    const int64_t span = by_rows ? b : (L + 255) / 256;              // rows, or 256-token blocks
+    const int np = (int)std::max<int64_t>(1, std::min<int64_t>(kHostPieces, span));
+    auto piece_lo = [&](int i) { return span * i / np; };
+    // per-token / per-row byte strides of each tensor
+    const size_t eb = elem_bytes(dims->dtype);
+    const size_t x_tok = eb * (size_t)(dims->nheads * dims->headdim);
+    const size_t dt_tok = eb * (size_t)dims->nheads;
+    const size_t bc_tok = eb * (size_t)(dims->ngroups * dims->dstate);
+    const size_t st_row = sizeof(float) * (size_t)(dims->nheads * dims->headdim * dims->dstate);
+
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    HostPipe* hp = nullptr;
+    int rc = host_pipe(&hp);
     if (rc != SSD_OK) return rc;
-    if ((s.x && cudaMemcpyAsync(y, dy, s.x, d2h, st) != cudaSuccess) ||
-        (final_state && cudaMemcpyAsync(final_state, dhT, s.st, d2h, st) != cudaSuccess))
-        return SSD_ERR_CUDA;
-    return SSD_OK;
+    bool ok = true;
+    auto chk = [&ok](cudaError_t e) { ok = ok && e == cudaSuccess; };
+    // the copy streams start after everything already on `stream` (which may still be using
+    // the arena from an earlier call)
+    chk(cudaEventRecord(hp->fork, st));
+    chk(cudaStreamWaitEvent(hp->in, hp->fork, 0));
+    chk(cudaStreamWaitEvent(hp->out, hp->fork, 0));
+    // A and D once, with the first piece
+    chk(cudaMemcpyAsync(dA, A, s.A, h2d, hp->in));
+    if (D) chk(cudaMemcpyAsync(dD, D, s.D, h2d, hp->in));
+    if (initial_state) chk(cudaMemcpyAsync(dh0, initial_state, s.st, h2d, hp->in));
+    for (int i = 0; i < np && ok && rc == SSD_OK; ++i) {
+        const int64_t lo = piece_lo(i), hi = piece_lo(i + 1);
+        ssd_dims pd = *dims;
+        size_t ox, odt, obc, n_x, n_dt, n_bc;   // byte offsets and sizes of the piece
+        if (by_rows) {
+            pd.batch = hi - lo;
+            ox = x_tok * (size_t)(lo * L);       n_x = x_tok * (size_t)(pd.batch * L);
+            odt = dt_tok * (size_t)(lo * L);     n_dt = dt_tok * (size_t)(pd.batch * L);
+            obc = bc_tok * (size_t)(lo * L);     n_bc = bc_tok * (size_t)(pd.batch * L);
+        } else {
+            const int64_t t0 = lo * 256, t1 = std::min<int64_t>(hi * 256, L);
+            pd.seqlen = t1 - t0;
+            ox = x_tok * (size_t)t0;             n_x = x_tok * (size_t)pd.seqlen;
+            odt = dt_tok * (size_t)t0;           n_dt = dt_tok * (size_t)pd.seqlen;
+            obc = bc_tok * (size_t)t0;           n_bc = bc_tok * (size_t)pd.seqlen;
+        }
+        const auto* cx = static_cast<const uint8_t*>(x);
+        const auto* cdt = static_cast<const uint8_t*>(dt);
+        const auto* cB = static_cast<const uint8_t*>(B);
+        const auto* cC = static_cast<const uint8_t*>(C);
+        if (n_x) chk(cudaMemcpyAsync(dx + ox, cx + ox, n_x, h2d, hp->in));
+        if (n_dt) chk(cudaMemcpyAsync(ddt + odt, cdt + odt, n_dt, h2d, hp->in));
+        if (n_bc) chk(cudaMemcpyAsync(dB + obc, cB + obc, n_bc, h2d, hp->in));
+        if (n_bc) chk(cudaMemcpyAsync(dC + obc, cC + obc, n_bc, h2d, hp->in));
+        chk(cudaEventRecord(hp->in_done[i], hp->in));
+        chk(cudaStreamWaitEvent(st, hp->in_done[i], 0));
+        if (!ok) break;
+        // the piece's entering and final state: its rows of h0 / hT, or (sequence pieces) the
+        // running state, which alternates between the two state buffers
+        const float* h_in;
+        float* h_out;
+        if (by_rows) {
+            h_in = initial_state ? dh0 + st_row / sizeof(float) * (size_t)lo : nullptr;
+            h_out = final_state ? dhT + st_row / sizeof(float) * (size_t)lo : nullptr;
+        } else {
+            h_in = i == 0 ? (initial_state ? dh0 : nullptr) : ((i & 1) ? dhT : dh0);
+            h_out = (np == 1 || i == np - 1) ? (final_state ? ((i & 1) ? dh0 : dhT) : nullptr)
+                                              : ((i & 1) ? dh0 : dhT);
+        }
+        rc = run(&pd, dx + ox, ddt + odt, dA, dB + obc, dC + obc, D ? dD : nullptr, h_in,
+                 chunk_size, dy + ox, h_out, dws, ws_bytes, stream, SSD_PATH_AUTO,
+                 /*clear_status=*/i == 0);
+        if (rc != SSD_OK) break;
+        chk(cudaEventRecord(hp->scan_done[i], st));
+        chk(cudaStreamWaitEvent(hp->out, hp->scan_done[i], 0));
+        if (n_x) chk(cudaMemcpyAsync(static_cast<uint8_t*>(y) + ox, dy + ox, n_x, d2h, hp->out));
+        if (by_rows && final_state)
+            chk(cudaMemcpyAsync(final_state + st_row / sizeof(float) * (size_t)lo,
+                                dhT + st_row / sizeof(float) * (size_t)lo,
+                                st_row * (size_t)pd.batch, d2h, hp->out));
+        if (!by_rows && final_state && i == np - 1)
+            chk(cudaMemcpyAsync(final_state, (i & 1) ? dh0 : dhT, s.st, d2h, hp->out));
+    }
+    // `stream` ends after both copy streams: the caller's synchronisation covers every copy
+    chk(cudaEventRecord(hp->join, hp->in));
+    chk(cudaStreamWaitEvent(st, hp->join, 0));
+    chk(cudaEventRecord(hp->join, hp->out));
+    chk(cudaStreamWaitEvent(st, hp->join, 0));
+    if (rc != SSD_OK) return rc;
+    return ok ? SSD_OK : SSD_ERR_CUDA;
 }
 
 // Sequence i of a packed batch as a one-row problem: tokens cu[i] .. cu[i+1] - 1.

@@ -157,15 +157,33 @@ def test_gpu_sequence_split_matches_one_call():
 
 # ---- API behaviour on the device -----------------------------------------------------------
 
-def test_host_entry_point_matches_device_entry_point():
-    inp = workloads.make_shape_inputs(2, 400, 4, 64, 128, 2, "bf16", seed=6, h0_mode="normal")
+# b, L, H, P, N, G, dtype, Q: pieces of batch rows (2 and 3 rows, uneven groups), pieces of
+# 256 tokens with the state carried (eight, the last one ragged; one short sequence), the
+# float32 chunked path
+HOST_CASES = [
+    (2, 400, 4, 64, 128, 2, "bf16", 128),
+    (3, 300, 2, 64, 128, 1, "bf16", 64),
+    (1, 2000, 4, 64, 128, 1, "bf16", 256),
+    (1, 100, 2, 64, 128, 1, "bf16", 128),
+    (1, 1100, 2, 32, 16, 1, "f32", 64),
+]
+
+
+@pytest.mark.parametrize("case", HOST_CASES, ids=lambda c: "b{}L{}H{}P{}N{}G{}{}Q{}".format(*c))
+@pytest.mark.parametrize("h0", [True, False], ids=["h0", "noh0"])
+def test_host_entry_point_pipeline_matches_oracle(case, h0):
+    """ssd_scan_fwd_host cuts the problem into pieces whose copies overlap the scans; its y and
+    final state match the oracle, and the device entry point within the same tolerance."""
+    b, L, H, P, N, G, dt, Q = case
+    inp = workloads.make_shape_inputs(b, L, H, P, N, G, dt, seed=L + b,
+                                      h0_mode="normal" if h0 else "none", d_mode="normal")
     pinned = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
     y_h, h_h = ssd_scan_fwd_host(pinned["x"], pinned["dt"], pinned["A"], pinned["B"],
-                                 pinned["C"], pinned["D"], pinned["h0"], chunk_size=128)
-    dev = to_device(inp)
-    y_d, h_d = run_gpu(dev, 128)
-    assert torch.equal(y_h, y_d.cpu())
-    assert torch.equal(h_h, h_d.cpu())
+                                 pinned["C"], pinned["D"], pinned["h0"], chunk_size=Q)
+    check_against_oracle(inp, y_h, h_h, use_h0=h0, what="host entry point")
+    y_d, h_d = run_gpu(to_device(inp), Q, use_h0=h0)
+    assert_close(y_h.float(), y_d.float().cpu(), dt, "host vs device y")
+    assert_close(h_h, h_d.cpu(), dt, "host vs device final state")
 
 
 def test_device_errors_raise():
