@@ -187,12 +187,17 @@ int ssd_scan_fwd_noalloc(const ssd_dims* dims,
  *   - nheads * headdim and ngroups * dstate elements must each be a multiple of 16 bytes, so
  *     that every sequence's x, y, B and C slices start on a 16-byte boundary
  *     (else SSD_ERR_UNSUPPORTED).
- *   - workspace: at least ssd_scan_varlen_workspace_bytes (the largest single sequence's
- *     need).  `path` as for ssd_scan_fwd_path, or SSD_PATH_AUTO.
- *   - Enqueues one scan per non-empty sequence on `stream`, in order, sharing the workspace.
- *     The status word is cleared once, so ssd_scan_get_status reports a device-side failure in
- *     any of them.  Returns as ssd_scan_fwd; every sequence is checked before anything is
- *     enqueued.
+ *   - workspace: at least ssd_scan_varlen_workspace_bytes.  `path` as for ssd_scan_fwd_path,
+ *     or SSD_PATH_AUTO.
+ *   - When every non-empty sequence takes the tensor-core path and there are at least two,
+ *     the sequences run concurrently on up to four library-owned streams of the current device
+ *     (longest first, each to the least loaded stream), each stream with its own slice of the
+ *     workspace and a grid of a quarter of the SMs; `stream` waits for all of them (events).
+ *     Otherwise one scan per non-empty sequence is enqueued on `stream`, in order, sharing the
+ *     workspace.
+ *   - The status word is cleared once and every scan reports into it, so ssd_scan_get_status
+ *     covers all of them.  Returns as ssd_scan_fwd; every sequence is checked before anything
+ *     is enqueued.
  */
 size_t ssd_scan_varlen_workspace_bytes(const ssd_dims* dims, const int64_t* cu_seqlens,
                                        int64_t nseq, int chunk_size, int path);

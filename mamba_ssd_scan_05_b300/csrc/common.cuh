@@ -32,6 +32,10 @@ struct ScanArgs {
     uint8_t* ws;               // workspace base (256-byte aligned)
     size_t ws_bytes;
     cudaStream_t stream;
+    // tensor-core path: at most this many CTAs (0: one per SM), and the status word to record
+    // a device-side failure in (null: the workspace's own)
+    int max_ctas = 0;
+    uint8_t* status = nullptr;
     // the gated RMSNorm fused into the output (tc128_launch with gated = 1 only): y receives
     // rmsnorm(scan) * w * silu(z) over groups of `group` features
     int gated = 0;
@@ -123,6 +127,8 @@ int tc128_launch(const ScanArgs& a);
 // Whether the d_state 128 kernel fuses the gated RMSNorm for this headdim and group size.
 bool tc128_gated_supports(int64_t P, int group);
 size_t tc_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t P, int64_t N, int Q);
+// The tensor-core workspace of a launch capped at `ctas` CTAs (hand-off slots for those only).
+size_t tc_workspace_bytes_ctas(int64_t N, int ctas);
 bool tc_supports(int32_t dtype, int64_t P, int64_t N, int Q);
 int tc_launch(const ScanArgs& a);
 

@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -70,7 +71,8 @@ struct Gate {
 int run(const ssd_dims* d, const void* x, const void* dt, const float* A, const void* B,
         const void* C, const float* D, const float* h0, int chunk_size, void* y, float* hT,
         void* workspace, size_t workspace_bytes, void* stream, int path,
-        bool clear_status = true, const Gate* gate = nullptr) {
+        bool clear_status = true, const Gate* gate = nullptr, int max_ctas = 0,
+        uint8_t* status = nullptr) {
     const int r = resolve(d, chunk_size, path);
     if (r < 0) return -r;
     if (!A || (d->seqlen > 0 && (!x || !dt || !B || !C || !y))) return SSD_ERR_INVALID;
@@ -80,7 +82,10 @@ int run(const ssd_dims* d, const void* x, const void* dt, const float* A, const 
         !aligned(h0, 4) || !aligned(hT, 4))
         return SSD_ERR_INVALID;
     if (!workspace || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
-    if (workspace_bytes < workspace_for(d, chunk_size, r)) return SSD_ERR_WORKSPACE;
+    const size_t need = (r == SSD_PATH_TC && max_ctas > 0)
+                            ? tc_workspace_bytes_ctas(d->dstate, max_ctas)
+                            : workspace_for(d, chunk_size, r);
+    if (workspace_bytes < need) return SSD_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the status word reports on this call only
     if (clear_status && cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess)
@@ -97,6 +102,8 @@ int run(const ssd_dims* d, const void* x, const void* dt, const float* A, const 
     a.dstate = d->dstate; a.ngroups = d->ngroups; a.dtype = d->dtype; a.chunk = chunk_size;
     a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.h0 = h0; a.y = y; a.hT = hT;
     a.ws = static_cast<uint8_t*>(workspace); a.ws_bytes = workspace_bytes; a.stream = st;
+    a.max_ctas = max_ctas;
+    a.status = status;
     if (gate) {
         a.gated = 1;
         a.z = gate->z;
@@ -142,10 +149,14 @@ constexpr int kHostPieces = 8;          // at most this many pieces per call
 // caller's stream, created on first use and kept for the life of the process.  Calls enqueue
 // under the mutex, so an event is never re-recorded before the previous call's waits on it
 // have been enqueued.
+constexpr int kVarlenLanes = 4;         // concurrent sequences of a packed batch
+constexpr int64_t kTileTokens = 128;    // the tensor-core kernels' tile (work estimate)
 struct HostPipe {
     cudaStream_t in = nullptr, out = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
     cudaEvent_t in_done[kHostPieces] = {}, scan_done[kHostPieces] = {};
+    cudaStream_t lane[kVarlenLanes] = {};
+    cudaEvent_t lane_done[kVarlenLanes] = {};
     bool ready = false;
 };
 std::mutex g_pipe_mutex;
@@ -165,6 +176,10 @@ int host_pipe(HostPipe** out) {
         for (int i = 0; i < kHostPieces; ++i)
             if (cudaEventCreateWithFlags(&hp.in_done[i], ef) != cudaSuccess ||
                 cudaEventCreateWithFlags(&hp.scan_done[i], ef) != cudaSuccess)
+                return SSD_ERR_CUDA;
+        for (int i = 0; i < kVarlenLanes; ++i)
+            if (cudaStreamCreateWithFlags(&hp.lane[i], cudaStreamNonBlocking) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.lane_done[i], ef) != cudaSuccess)
                 return SSD_ERR_CUDA;
         hp.ready = true;
     }
@@ -348,6 +363,29 @@ static int check_varlen(const ssd_dims* dims, const int64_t* cu, int64_t nseq) {
     return SSD_OK;
 }
 
+// A packed batch whose non-empty sequences all take the tensor-core path, and more than one,
+// runs them concurrently: on up to kVarlenLanes streams, each with its own workspace slice
+// (hand-off slots for kVarlenCtas CTAs) and a grid of a quarter of the SMs.  With fewer CTAs
+// per sequence a short sequence's chains are not cut into look-back pieces, and the lanes
+// overlap each other's pipeline fill and drain.  Returns the number of lanes, or 0 for the
+// sequential form (one launch after another on the caller's stream, one shared workspace).
+constexpr int kVarlenCtas = 64;
+static int varlen_lanes(const ssd_dims* dims, const int64_t* cu, int64_t nseq, int chunk_size,
+                        int path) {
+    int64_t busy = 0;
+    for (int64_t i = 0; i < nseq; ++i) {
+        ssd_dims di;
+        varlen_dims(dims, cu, i, &di);
+        if (di.seqlen == 0) continue;
+        if (resolve(&di, chunk_size, path) != SSD_PATH_TC) return 0;
+        ++busy;
+    }
+    return busy < 2 ? 0 : (int)std::min<int64_t>(kVarlenLanes, busy);
+}
+static size_t varlen_slice_bytes(const ssd_dims* dims) {
+    return align_up(tc_workspace_bytes_ctas(dims->dstate, kVarlenCtas), 256);
+}
+
 size_t ssd_scan_varlen_workspace_bytes(const ssd_dims* dims, const int64_t* cu_seqlens,
                                        int64_t nseq, int chunk_size, int path) {
     if (check_varlen(dims, cu_seqlens, nseq) != SSD_OK) return 0;
@@ -360,6 +398,8 @@ size_t ssd_scan_varlen_workspace_bytes(const ssd_dims* dims, const int64_t* cu_s
         if (r < 0) return 0;
         need = std::max(need, workspace_for(&di, chunk_size, r));
     }
+    const int lanes = varlen_lanes(dims, cu_seqlens, nseq, chunk_size, path);
+    if (lanes > 0) need = (size_t)lanes * varlen_slice_bytes(dims);
     return std::max(need, (size_t)kWsHeaderBytes);
 }
 
@@ -384,32 +424,71 @@ int ssd_scan_fwd_varlen(const ssd_dims* dims, const int64_t* cu_seqlens, int64_t
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return SSD_ERR_CUDA;
     const size_t state_elems = (size_t)(H * P * N);
-    for (int64_t i = 0; i < nseq; ++i) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    // sequence i on `lane_st` with the workspace `wsp` of `wsb` bytes
+    auto scan_one = [&](int64_t i, cudaStream_t lane_st, uint8_t* wsp, size_t wsb,
+                        int max_ctas) -> int {
         ssd_dims di;
         varlen_dims(dims, cu_seqlens, i, &di);
         const int64_t t0 = cu_seqlens[i];
-        const uint8_t* xb = static_cast<const uint8_t*>(x);
-        const uint8_t* dtb = static_cast<const uint8_t*>(dt);
-        const uint8_t* Bb = static_cast<const uint8_t*>(B);
-        const uint8_t* Cb = static_cast<const uint8_t*>(C);
-        uint8_t* yb = static_cast<uint8_t*>(y);
         const float* h0 = initial_state ? initial_state + i * state_elems : nullptr;
         float* hT = final_state ? final_state + i * state_elems : nullptr;
         if (di.seqlen == 0) {   // an empty sequence: its final state is its initial state
-            if (!hT) continue;
+            if (!hT) return SSD_OK;
             const size_t sb = sizeof(float) * state_elems;
-            const cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, sb, cudaMemcpyDeviceToDevice, st)
-                                     : cudaMemsetAsync(hT, 0, sb, st);
-            if (e != cudaSuccess) return SSD_ERR_CUDA;
-            continue;
+            const cudaError_t e = h0 ? cudaMemcpyAsync(hT, h0, sb, cudaMemcpyDeviceToDevice, lane_st)
+                                     : cudaMemsetAsync(hT, 0, sb, lane_st);
+            return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
         }
-        rc = run(&di, xb + eb * (size_t)(t0 * H * P), dtb + eb * (size_t)(t0 * H), A,
-                 Bb + eb * (size_t)(t0 * G * N), Cb + eb * (size_t)(t0 * G * N), D, h0,
-                 chunk_size, yb + eb * (size_t)(t0 * H * P), hT, workspace, workspace_bytes,
-                 stream, path, /*clear_status=*/false);
-        if (rc != SSD_OK) return rc;
+        return run(&di, static_cast<const uint8_t*>(x) + eb * (size_t)(t0 * H * P),
+                   static_cast<const uint8_t*>(dt) + eb * (size_t)(t0 * H), A,
+                   static_cast<const uint8_t*>(B) + eb * (size_t)(t0 * G * N),
+                   static_cast<const uint8_t*>(C) + eb * (size_t)(t0 * G * N), D, h0,
+                   chunk_size, static_cast<uint8_t*>(y) + eb * (size_t)(t0 * H * P), hT, wsp,
+                   wsb, lane_st, path, /*clear_status=*/false, nullptr, max_ctas, ws);
+    };
+    const int lanes = varlen_lanes(dims, cu_seqlens, nseq, chunk_size, path);
+    if (lanes == 0) {
+        for (int64_t i = 0; i < nseq; ++i) {
+            rc = scan_one(i, st, ws, workspace_bytes, 0);
+            if (rc != SSD_OK) return rc;
+        }
+        return SSD_OK;
     }
-    return SSD_OK;
+    // concurrent form: longest sequences first, each to the lane with the least work so far
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    const int ctas = std::max(1, std::min(kVarlenCtas, nsm / lanes));
+    const size_t slice = varlen_slice_bytes(dims);
+    std::vector<int64_t> order((size_t)nseq);
+    for (int64_t i = 0; i < nseq; ++i) order[(size_t)i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
+        return cu_seqlens[a + 1] - cu_seqlens[a] > cu_seqlens[b + 1] - cu_seqlens[b];
+    });
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    HostPipe* hp = nullptr;
+    rc = host_pipe(&hp);
+    if (rc != SSD_OK) return rc;
+    bool ok = cudaEventRecord(hp->fork, st) == cudaSuccess;
+    for (int l = 0; l < lanes && ok; ++l) ok = cudaStreamWaitEvent(hp->lane[l], hp->fork, 0) == cudaSuccess;
+    int64_t load[kVarlenLanes] = {};
+    for (size_t k = 0; k < order.size() && ok && rc == SSD_OK; ++k) {
+        const int64_t i = order[k];
+        int l = 0;
+        for (int m = 1; m < lanes; ++m)
+            if (load[m] < load[l]) l = m;
+        load[l] += (cu_seqlens[i + 1] - cu_seqlens[i] + kTileTokens - 1) / kTileTokens + 1;
+        rc = scan_one(i, hp->lane[l], ws + (size_t)l * slice, slice, ctas);
+    }
+    // `stream` continues after every lane, also on an error (nothing is left unordered)
+    for (int l = 0; l < lanes; ++l) {
+        ok = cudaEventRecord(hp->lane_done[l], hp->lane[l]) == cudaSuccess && ok;
+        ok = cudaStreamWaitEvent(st, hp->lane_done[l], 0) == cudaSuccess && ok;
+    }
+    if (rc != SSD_OK) return rc;
+    return ok ? SSD_OK : SSD_ERR_CUDA;
 }
 
 int ssd_step_fwd(const ssd_dims* dims, const void* x, const void* dt, const float* A,

@@ -614,6 +614,7 @@ int launch_ns(const ScanArgs& a) {
     p.n_units = a.batch * a.nheads * p.n_ps;
     const int64_t total = p.n_units * p.n_tiles;
     p.n_ctas = (int)std::min<int64_t>(std::min(nsm, kMaxCtas), total);
+    if (a.max_ctas > 0) p.n_ctas = std::min(p.n_ctas, a.max_ctas);
     // Without a state-only pass, a range's head piece is published before its successor's
     // tail piece is needed as long as every range is longer than a chain.
     p.pass1_mode = (total / p.n_ctas) > p.n_tiles ? 0 : 1;
@@ -621,7 +622,7 @@ int launch_ns(const ScanArgs& a) {
     p.A = a.A; p.D = a.D; p.h0 = a.h0;
     p.y = static_cast<__nv_bfloat16*>(a.y);
     p.hT = a.hT;
-    p.ws = a.ws;
+    p.ws = a.status ? a.status : a.ws;
     p.flags = reinterpret_cast<int*>(a.ws + kWsHeaderBytes);
     p.slots = reinterpret_cast<float*>(a.ws + kWsHeaderBytes + flags_bytes());
     p.budget = tc_wait_budget();
@@ -651,6 +652,10 @@ bool tc_supports(int32_t dtype, int64_t P, int64_t N, int Q) {
 
 size_t tc_workspace_bytes(int64_t, int64_t, int64_t, int64_t, int64_t N, int) {
     return kWsHeaderBytes + flags_bytes() + slots_bytes(N);
+}
+
+size_t tc_workspace_bytes_ctas(int64_t N, int ctas) {
+    return kWsHeaderBytes + flags_bytes() + sizeof(float) * 2 * (size_t)ctas * kPS * (size_t)N;
 }
 
 int tc_launch(const ScanArgs& a) {

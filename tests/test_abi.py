@@ -140,8 +140,13 @@ def test_step_argument_checks_need_no_gpu(lib):
 def test_varlen_workspace_checks_offsets(lib):
     import mamba_ssd_scan_05_b300 as m
     d = dims(b=1, L=300, H=8, P=64, N=128)
+    # two non-empty tensor-core sequences run concurrently: a workspace slice per lane, each
+    # with hand-off slots for 64 CTAs (2 x 64 x 64 x 128 floats)
     good = m.ssd_scan_varlen_workspace_bytes(d, [0, 100, 100, 300], 128)
-    assert good >= m.ssd_scan_workspace_bytes(dims(b=1, L=200, H=8, P=64, N=128), 128)
+    assert good >= 2 * (2 * 64 * 64 * 128 * 4)
+    # one non-empty sequence runs as a plain scan: the whole scan workspace
+    one = m.ssd_scan_varlen_workspace_bytes(dims(b=1, L=200, H=8, P=64, N=128), [0, 0, 200], 128)
+    assert one >= m.ssd_scan_workspace_bytes(dims(b=1, L=200, H=8, P=64, N=128), 128)
     assert m.ssd_scan_varlen_workspace_bytes(d, [0, 100, 299], 128) == 0      # wrong total
     assert m.ssd_scan_varlen_workspace_bytes(d, [0, 200, 100, 300], 128) == 0  # decreasing
     assert m.ssd_scan_varlen_workspace_bytes(dims(b=2, L=300), [0, 300], 128) == 0  # batch != 1

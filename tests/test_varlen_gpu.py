@@ -43,12 +43,20 @@ def test_mixed_lengths_match_the_oracle_per_sequence(path):
     check_each_sequence(inp, y, hT)
 
 
-def test_packed_equals_separate_calls_bitwise():
-    lengths = [513, 77, 256, 1200]
+def test_packed_matches_separate_calls_and_repeats_bitwise():
+    """The packed call (sequences on concurrent streams, capped grids) agrees with one call per
+    sequence within rounding, matches the oracle per sequence, and gives the same bits when
+    repeated: the work plan and the lane assignment are fixed, not timing-dependent."""
+    lengths = [513, 77, 256, 1200, 3000, 5, 640]
     inp = workloads.make_varlen_inputs(lengths, 4, 64, 128, 1, "bf16", seed=6)
     dev = cuda(inp)
-    y, hT = ssd_scan_fwd_varlen(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"],
-                                inp["cu_seqlens"], dev["D"], dev["h0"], chunk_size=256)
+    args = (dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], inp["cu_seqlens"], dev["D"],
+            dev["h0"])
+    y, hT = ssd_scan_fwd_varlen(*args, chunk_size=256)
+    y2, hT2 = ssd_scan_fwd_varlen(*args, chunk_size=256)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2) and torch.equal(hT, hT2)
+    check_each_sequence(inp, y, hT)
     cu = inp["cu_seqlens"]
     for i in range(len(lengths)):
         a, b = cu[i], cu[i + 1]
@@ -56,7 +64,8 @@ def test_packed_equals_separate_calls_bitwise():
         yi, hi = ssd_scan_fwd(sl["x"], sl["dt"], dev["A"], sl["B"], sl["C"], dev["D"],
                               dev["h0"][i:i + 1].contiguous(), chunk_size=256)
         torch.cuda.synchronize()
-        assert torch.equal(yi, y[:, a:b]) and torch.equal(hi[0], hT[i]), i
+        assert_close(y[:, a:b].float().cpu(), yi.float().cpu(), "bf16", f"seq {i} y")
+        assert_close(hT[i:i + 1].cpu(), hi.cpu(), "bf16", f"seq {i} state")
 
 
 def test_float32_and_no_initial_states():
