@@ -57,6 +57,7 @@
 // status word, makes every role stop, drains in-flight copies and MMAs (with a fixed limit of
 // their own) and frees TMEM before exit.
 #include "tc_common.cuh"
+#include "tc_state.cuh"
 
 namespace ssd {
 namespace {
@@ -107,12 +108,13 @@ struct K3 {
 
 // Warp 0, one lane: B and C tiles of every tile of the CTA's plan into the B / C ring (a
 // state-only tile needs B only).
+template <bool kExt>
 __device__ __forceinline__ void role_bc_producer(const Plan& plan, Small& sm, const TcParams& p,
                                                  uint8_t* smem, const CUtensorMap* tmB,
                                                  const CUtensorMap* tmC) {
     using K = K3;
     int nt = 0;
-    for (Cursor c = first_tile(plan, sm, p); c.valid; advance_p(c, plan, sm, p), ++nt) {
+    for (Cursor c = first_tile<kExt>(plan, sm, p); c.valid; advance_p<kExt>(c, plan, sm, p), ++nt) {
         const int s = nt % K::kBCStages;
         const uint32_t use = nt / K::kBCStages;
         if (!wait_bar_p(&sm.bc_empty[s], (use & 1u) ^ 1u, sm, p)) break;
@@ -136,6 +138,7 @@ __device__ __forceinline__ void role_bc_producer(const Plan& plan, Small& sm, co
 }
 
 // Warp 2, all lanes: the x tile (TMA) and the tile's decay factors and mode (DtSlot).
+template <bool kExt>
 __device__ __forceinline__ void role_x_producer(const Plan& plan, Small& sm, const TcParams& p,
                                                 uint8_t* smem, DtSlot* slots,
                                                 const CUtensorMap* tmX, int lane) {
@@ -155,7 +158,7 @@ __device__ __forceinline__ void role_x_producer(const Plan& plan, Small& sm, con
     // memory latency overlaps this tile's work
     float dn[4] = {0.f, 0.f, 0.f, 0.f};
     bool have_next = false;
-    for (Cursor c = first_tile(plan, sm, p); c.valid; advance_p(c, plan, sm, p), ++nt) {
+    for (Cursor c = first_tile<kExt>(plan, sm, p); c.valid; advance_p<kExt>(c, plan, sm, p), ++nt) {
         float d0[4];
         if (have_next) {
 #pragma unroll
@@ -195,6 +198,7 @@ __device__ __forceinline__ void role_x_producer(const Plan& plan, Small& sm, con
 // factored tile, the raw x tile on a fallback tile), then G_{k+1} = C B^T of the next tile once
 // the compute warps have read G_k.  Per state-only tile: S^T_k alone.  Each K = 128 GEMM goes
 // out as one block of 8 back-to-back MMAs.
+template <bool kExt>
 __device__ __forceinline__ void role_mma(const Plan& plan, Small& sm, const TcParams& p,
                                          const DtSlot* slots, uint32_t sbase, uint32_t tmem,
                                          int lane) {
@@ -220,7 +224,7 @@ __device__ __forceinline__ void role_mma(const Plan& plan, Small& sm, const TcPa
     int nt = 0, j = 0;        // tiles issued, full (non state-only) tiles issued
     int nf = 0;               // fallback full tiles issued
     bool g_ahead = false;     // G of the current tile was issued during the previous tile
-    Cursor c = first_tile(plan, sm, p);
+    Cursor c = first_tile<kExt>(plan, sm, p);
     for (; c.valid; ++nt) {
         const int s = nt % K::kBCStages;
         const int xs = nt % K::kXSt;
@@ -229,7 +233,7 @@ __device__ __forceinline__ void role_mma(const Plan& plan, Small& sm, const TcPa
         const bool next_full =
             (c.k + 1 < c.it.k1)
                 ? !c.it.pass1
-                : (c.item + 1 < plan.n_items && !plan_item(plan, c.item + 1, p.n_tiles).pass1);
+                : (c.item + 1 < plan.n_items && !plan_item<kExt>(plan, c.item + 1, p.n_tiles).pass1);
         if (full_tile && !g_ahead && !issue_G(nt, j)) break;
         g_ahead = false;
         // chunk state S^T = B^T Xs, once the compute warps have built Xs and read S^T_{k-1}
@@ -249,7 +253,7 @@ __device__ __forceinline__ void role_mma(const Plan& plan, Small& sm, const TcPa
             mma_commit_e(&sm.xt_empty);
             mma_commit_e(&sm.bc_empty[s]);
             mma_commit_e(&sm.x_empty[xs]);
-            advance_p(c, plan, sm, p);
+            advance_p<kExt>(c, plan, sm, p);
             continue;
         }
         // the tile's mode, written by the decay producer before x_full completed
@@ -288,7 +292,7 @@ __device__ __forceinline__ void role_mma(const Plan& plan, Small& sm, const TcPa
             g_ahead = true;
         }
         ++j;
-        advance_p(c, plan, sm, p);
+        advance_p<kExt>(c, plan, sm, p);
     }
     // every MMA issued above has completed once this barrier's phase 0 completes
     mma_commit_e(&sm.mma_done);
@@ -507,7 +511,7 @@ __device__ __forceinline__ void ht_write_scaled(const float (&h)[16], float s, u
 // Warps 4-19: compute warpgroup wg (headdim columns c0 = 16 wg ..), lane quarter q (TMEM lanes,
 // tile rows and state rows 32q .. 32q+31).  Per tile: the scaled x tile, this tile's P block,
 // the previous tile's y, the state.  Returns false on a timeout or abort.
-template <bool kGated>
+template <bool kGated, bool kExt>
 __device__ __forceinline__ bool role_compute(const Plan& plan, Small& sm, const TcParams& p,
                                              uint8_t* smem, const DtSlot* slots, uint32_t tmem,
                                              int w, int lane) {
@@ -527,7 +531,7 @@ __device__ __forceinline__ bool role_compute(const Plan& plan, Small& sm, const 
     int d_u = -1;
     float Dh = 0.f;
     float item_logd = 0.f;                   // sum of log2 tile decays over the item
-    for (Cursor c = first_tile(plan, sm, p); c.valid; advance(c, plan, sm, p), ++nt) {
+    for (Cursor c = first_tile<kExt>(plan, sm, p); c.valid; advance<kExt>(c, plan, sm, p), ++nt) {
         const UnitCoords& uc = c.uc;
         const bool full_tile = !c.it.pass1;
         const int xs = nt % K::kXSt;
@@ -730,7 +734,7 @@ __device__ __forceinline__ bool role_compute(const Plan& plan, Small& sm, const 
 
 // ------------------------------------------------------------------- the kernel --------------
 
-template <bool kGated>
+template <bool kGated, bool kExt>
 __global__ void __launch_bounds__(K3::kThreads, 1)
     ssd_tc128_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmB,
@@ -770,7 +774,7 @@ __global__ void __launch_bounds__(K3::kThreads, 1)
         for (int i = 0; i < 4; ++i) mbar_init(&sm.red_bar[i], 128);
         mbar_init(&sm.mma_done, 1);
         sm.abort_flag = 0;
-        sm.plan = plan::make_plan(p.n_units, p.n_tiles, p.n_ctas, p.pass1_mode, blockIdx.x);
+        sm.plan = plan::make_plan<kExt>(p.n_units, p.n_tiles, p.n_ctas, p.pass1_mode, blockIdx.x);
         const int us[3] = {sm.plan.u0, sm.plan.u1, sm.plan.f_lo};
         int* dst[3] = {sm.uc_u0, sm.uc_u1, sm.uc_flo};
         for (int i = 0; i < 3; ++i) {
@@ -819,15 +823,15 @@ __global__ void __launch_bounds__(K3::kThreads, 1)
     if (warp < kWarpC) {
         regs_dec<K::kRegsProducer>();
         if (warp == kWarpTma) {
-            if (lane == 0) role_bc_producer(plan, sm, p, smem, &tmB, &tmC);
+            if (lane == 0) role_bc_producer<kExt>(plan, sm, p, smem, &tmB, &tmC);
         } else if (warp == kWarpDt) {
-            role_x_producer(plan, sm, p, smem, slots, &tmX, lane);
+            role_x_producer<kExt>(plan, sm, p, smem, slots, &tmX, lane);
         } else if (warp == kWarpMma) {
-            role_mma(plan, sm, p, slots, sbase, tmem, lane);
+            role_mma<kExt>(plan, sm, p, slots, sbase, tmem, lane);
         }
     } else {
         regs_inc<K::kRegsCompute>();
-        role_compute<kGated>(plan, sm, p, smem, slots, tmem, warp - kWarpC, lane);
+        role_compute<kGated, kExt>(plan, sm, p, smem, slots, tmem, warp - kWarpC, lane);
     }
 
     // single-lane roles (B / C TMA) reconverge their warp before the CTA barrier
@@ -846,17 +850,22 @@ template <bool kGated>
 int launch128(const ScanArgs& a, const TcParams& p) {
     using K = K3;
     constexpr size_t smem = kGated ? K::kSmemBytesGated : K::kSmemBytes;
+    // Ranges shorter than chains: the state-only passes run as a kernel of their own
+    // (tc_state.cuh), then the scan instance whose plan leaves them out (kExt), which finds
+    // every state it looks back for already published.
+    const bool ext = p.pass1_mode == 1;
+    auto kernel = ext ? ssd_tc128_kernel<kGated, true> : ssd_tc128_kernel<kGated, false>;
     // the setmaxnreg split must fit in the registers the kernel is launched with: check what
-    // the compiler gave it before the first launch (a split that does not fit would never
-    // complete)
-    static int regs_ok = -1;
-    if (regs_ok < 0) {
+    // the compiler gave each instance before its first launch (a split that does not fit would
+    // never complete)
+    static int regs_ok[2] = {-1, -1};
+    if (regs_ok[ext] < 0) {
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, ssd_tc128_kernel<kGated>) != cudaSuccess)
-            return SSD_ERR_CUDA;
-        regs_ok = (fa.numRegs == K::kRegsLaunch && fa.maxThreadsPerBlock >= K::kThreads) ? 1 : 0;
+        if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return SSD_ERR_CUDA;
+        regs_ok[ext] =
+            (fa.numRegs == K::kRegsLaunch && fa.maxThreadsPerBlock >= K::kThreads) ? 1 : 0;
     }
-    if (!regs_ok) return SSD_ERR_UNSUPPORTED;
+    if (!regs_ok[ext]) return SSD_ERR_UNSUPPORTED;
     CUtensorMap tmX, tmB, tmC;
     if (!make_map(&tmX, a.x, a.headdim, a.nheads, a.seqlen, a.batch) ||
         !make_map(&tmB, a.B, a.dstate, a.ngroups, a.seqlen, a.batch) ||
@@ -865,10 +874,14 @@ int launch128(const ScanArgs& a, const TcParams& p) {
     if (cudaMemsetAsync(p.flags, 0, sizeof(int) * kFlagsPerCta * (size_t)p.n_ctas, a.stream) !=
         cudaSuccess)
         return SSD_ERR_CUDA;
-    if (cudaFuncSetAttribute(ssd_tc128_kernel<kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
         return SSD_ERR_CUDA;
-    ssd_tc128_kernel<kGated><<<(unsigned)p.n_ctas, K::kThreads, smem, a.stream>>>(tmX, tmB, tmC, p);
+    if (ext) {
+        const int rc = tc128_state_launch(tmX, tmB, p, a.stream);
+        if (rc != SSD_OK) return rc;
+    }
+    kernel<<<(unsigned)p.n_ctas, K::kThreads, smem, a.stream>>>(tmX, tmB, tmC, p);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -35,11 +35,16 @@ struct Item {
 // the piece with a successor, in pass1 mode], [head piece], [whole chains], [tail piece], so
 // the state a successor needs is published as early as possible and the state a range needs
 // is consumed as late as possible.
+//
+// kExt (the plan of a kernel launched after the separate state-only pass, tc_state.cuh): the
+// same plan as pass1_mode 1 without the state-only items, which that pass has run already,
+// publishing what they publish.
 struct Plan {
     int u0, u1, f_lo, n_full, n_items;
     int k0, k1, n_pre, middle, p1;
 };
 
+template <bool kExt = false>
 SSD_HD Plan make_plan(int64_t n_units, int n_tiles, int n_ctas, int pass1_mode, int cta) {
     Plan pl;
     pl.u0 = pl.u1 = pl.f_lo = pl.n_full = pl.n_items = 0;
@@ -55,14 +60,14 @@ SSD_HD Plan make_plan(int64_t n_units, int n_tiles, int n_ctas, int pass1_mode, 
     pl.k1 = (int)((end - 1) % T + 1);
     if (pl.u0 == pl.u1 && pl.k0 > 0 && pl.k1 < T) {     // middle piece of one chain
         pl.middle = 1;
-        pl.n_pre = pl.p1;
+        pl.n_pre = kExt ? 0 : pl.p1;
         pl.n_items = pl.n_pre + 1;
         return pl;
     }
     // head piece of chain u1 (starts at tile 0, ends before T); tail piece of chain u0
     const bool head = (pl.u0 == pl.u1) ? (pl.k0 == 0 && pl.k1 < T) : (pl.k1 < T);
     const bool tail = pl.k0 > 0;
-    pl.n_pre = head ? 1 + pl.p1 : 0;
+    pl.n_pre = head ? 1 + (kExt ? 0 : pl.p1) : 0;
     const int f_first = tail ? pl.u0 + 1 : pl.u0;
     const int f_last = head ? pl.u1 - 1 : pl.u1;
     if (f_last >= f_first) {
@@ -73,13 +78,14 @@ SSD_HD Plan make_plan(int64_t n_units, int n_tiles, int n_ctas, int pass1_mode, 
     return pl;
 }
 
+template <bool kExt = false>
 SSD_HD Item plan_item(const Plan& pl, int i, int T) {
     if (pl.middle) {
         if (pl.n_pre > 0 && i == 0) return Item{pl.u0, pl.k0, pl.k1, 1, kInitZero, kFinAgg};
         return Item{pl.u0, pl.k0, pl.k1, 0, kInitLookback, kFinIncl};
     }
     if (i < pl.n_pre) {
-        if (pl.p1 && i == 0) return Item{pl.u1, 0, pl.k1, 1, kInitH0, kFinIncl};
+        if (!kExt && pl.p1 && i == 0) return Item{pl.u1, 0, pl.k1, 1, kInitH0, kFinIncl};
         return Item{pl.u1, 0, pl.k1, 0, kInitH0, pl.p1 ? kFinNone : kFinIncl};
     }
     i -= pl.n_pre;

@@ -47,10 +47,30 @@ void check(long U, int T, int C, int p1) {
     std::vector<Look> looks;
     for (int c = 0; c < C; ++c) {
         const long start = (long)c * total / C, end = (long)(c + 1) * total / C;
-        const Plan pl = make_plan(U, T, C, p1, c);
+        // mode 2: the plan of the kernel launched after the separate state-only pass
+        const Plan pl = p1 == 2 ? make_plan<true>(U, T, C, 1, c) : make_plan(U, T, C, p1, c);
         int pub_unit = -1;
+        if (p1 == 2) {
+            // the separate state-only kernel runs mode 1's state-only items of this range and
+            // publishes what they publish; the plan itself must hold none of them
+            const Plan ext = make_plan(U, T, C, 1, c);
+            for (int i = 0; i < ext.n_items; ++i) {
+                const Item it = plan_item(ext, i, T);
+                if (!it.pass1) continue;
+                Pub& pb = (it.fin == kFinIncl) ? incl[c] : agg[c];
+                if (pb.set) fail("two publications of one kind", U, T, C, p1, c, i);
+                pb.set = true;
+                pb.u = it.u;
+                pb.k0 = it.k0;
+                pb.k1 = it.k1;
+                pub_unit = it.u;
+            }
+            for (int i = 0; i < pl.n_items; ++i)
+                if (plan_item<true>(pl, i, T).pass1)
+                    fail("state-only item in mode 2", U, T, C, p1, c, i);
+        }
         for (int i = 0; i < pl.n_items; ++i) {
-            const Item it = plan_item(pl, i, T);
+            const Item it = p1 == 2 ? plan_item<true>(pl, i, T) : plan_item(pl, i, T);
             if (it.u < 0 || it.u >= U || it.k0 < 0 || it.k1 > T || it.k0 >= it.k1) {
                 fail("item range", U, T, C, p1, c, i);
                 continue;
@@ -114,7 +134,7 @@ void check(long U, int T, int C, int p1) {
         for (int jp = lk.cta - 1; jp >= 0 && !done; --jp) {
             const Pub& in = incl[jp];
             const Pub& ag = agg[jp];
-            if (!lookback_uses_aggregate(U, T, C, p1, jp, lk.u)) {
+            if (!lookback_uses_aggregate(U, T, C, p1 == 2 ? 1 : p1, jp, lk.u)) {
                 if (!(in.set && in.u == lk.u && in.k1 == pos)) {
                     fail("look-back wants an inclusive state that is not there", U, T, C, p1,
                          lk.cta, jp);
@@ -149,7 +169,7 @@ int main() {
             for (int C0 : ctas) {
                 const long total = U * T;
                 const int C = (int)(C0 < total ? C0 : total);   // the launcher's clamp
-                for (int p1 = 0; p1 < 2; ++p1) {
+                for (int p1 = 0; p1 < 3; ++p1) {
                     check(U, T, C, p1);
                     ++cases;
                 }

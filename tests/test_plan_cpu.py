@@ -28,6 +28,9 @@ MUTANTS = {
     # a head piece that publishes nothing
     "head_unpublished": ("return Item{pl.u1, 0, pl.k1, 0, kInitH0, pl.p1 ? kFinNone : kFinIncl};",
                          "return Item{pl.u1, 0, pl.k1, 0, kInitH0, kFinNone};"),
+    # mode 2 keeping the head's state-only item that the separate kernel runs
+    "mode2_keeps_state_only_item": ("pl.n_pre = head ? 1 + (kExt ? 0 : pl.p1) : 0;",
+                                    "pl.n_pre = head ? 1 + pl.p1 : 0;"),
     # the tail piece starting from the initial state instead of looking back
     "tail_no_look_back": ("return Item{pl.u0, pl.k0, (pl.u0 == pl.u1) ? pl.k1 : T, 0, kInitLookback, kFinFinal};",
                           "return Item{pl.u0, pl.k0, (pl.u0 == pl.u1) ? pl.k1 : T, 0, kInitH0, kFinFinal};"),

@@ -30,8 +30,10 @@ def test_wait_limit_runs_out_then_next_call_is_clean(shape):
     ws = torch.empty(ssd_scan_workspace_bytes(dims, Q, SSD_PATH_TC), dtype=torch.uint8,
                      device="cuda")
     args = (dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["h0"])
-    # a limit of 200 cycles: shorter than a TMA load from HBM or one tile's GEMMs, so some wait
-    # of every CTA gives up
+    # a limit of 200 cycles: shorter than a TMA load from HBM or one tile's GEMMs.  Both shapes
+    # cut chains across CTAs: for N = 128 the separate state-only pass gives up at its first
+    # copy and publishes nothing, and the scan's look-back then gives up too; for N = 256 the
+    # scan's own waits do.
     ssd_scan_set_wait_cycles(200)
     try:
         ssd_scan_fwd(*args, chunk_size=Q, path=SSD_PATH_TC, workspace=ws)
