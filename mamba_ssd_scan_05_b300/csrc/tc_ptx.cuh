@@ -129,6 +129,21 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared memory (both 4-byte aligned), in this thread's
+// current cp.async group; commit closes the group; wait until at most N groups are pending.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Bulk groups of this thread's TMA stores: close the current group; wait until at most N
 // groups are still reading shared memory; wait until every group has completed.
 __device__ __forceinline__ void bulk_commit() {

@@ -25,6 +25,11 @@
 #pragma once
 
 #include "tc_common.cuh"
+// Timing hook for profiling builds: a no-op unless the build defines
+// SSD_ST_TRACE_POINT(event, tile) (then it records a per-role clock64 timeline).
+#ifndef SSD_ST_TRACE_POINT
+#define SSD_ST_TRACE_POINT(event, tile) ((void)0)
+#endif
 
 namespace ssd {
 namespace {
@@ -49,7 +54,9 @@ struct SK {
     static constexpr uint32_t kOffStage = 0;
     static constexpr uint32_t kOffXs = kStages * kStageBytes;           // 2 buffers
     static constexpr uint32_t kOffSlot = kOffXs + 2 * kTileBytes;
-    static constexpr uint32_t kOffBar = kOffSlot + kStages * sizeof(StSlot);
+    static constexpr uint32_t kOffDt = kOffSlot + kStages * sizeof(StSlot);   // dt ring
+    static constexpr int kDtRing = 8, kDtAhead = 4;     // ring tiles; tiles loaded ahead
+    static constexpr uint32_t kOffBar = kOffDt + kDtRing * kTile * 4;
     static constexpr size_t kSmem = kOffBar + 256 + 1024;             // + alignment slack
     static constexpr uint32_t kTmemCols = 64;                          // S^T [128 x 64]
 };
@@ -90,6 +97,28 @@ __device__ __forceinline__ bool sp_wait(uint64_t* bar, uint32_t parity, StBars& 
     return __all_sync(0xffffffffu, ok);
 }
 
+// A tile's log2 cumsum (4 tokens per lane) as a float32 warp scan, and (returned) its last
+// value.  The state pass needs weights and group decays that agree with each other, not the
+// scan kernel's bit-exact 64-bit form; the float scan's rounding (about 1e-5 in log2 over a
+// tile) is far below bf16's.
+__device__ __forceinline__ float tile_scan2f(const float (&d0)[4], float A2, int lane,
+                                             float (&c2)[4]) {
+    float cs[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cs[i] = (i == 0 ? 0.f : cs[i - 1]) + d0[i] * A2;
+    float incl = cs[3];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c2[i] = excl + cs[i];
+    return __shfl_sync(0xffffffffu, incl, 31);
+}
+
 // The CTA's state-only item under plan mode 1 (the piece whose state it must publish), if any.
 __device__ __forceinline__ bool pass1_item(const TcParams& p, Item& out) {
     const Plan pl = plan::make_plan(p.n_units, p.n_tiles, p.n_ctas, 1, (int)blockIdx.x);
@@ -110,40 +139,56 @@ __device__ __forceinline__ void sp_producer(const Item& it, const UnitCoords& uc
                                             const CUtensorMap* tmX, const CUtensorMap* tmB,
                                             int lane) {
     const float A2 = p.A[uc.h] * kLog2e;
-    // dt of tile k, 4 consecutive tokens per lane, kept as the raw bf16 bits until used: a load
-    // whose value is converted at once would stall the warp for its whole latency
-    auto load_dt = [&](int k, uint32_t (&r)[4]) {
+    // dt of tile k, 4 consecutive tokens per lane, copied asynchronously (cp.async) into a ring
+    // in shared memory kDtAhead tiles ahead: the aligned 4-byte word holding each token's bf16
+    // value (it lies inside the tensor's allocation, whose bounds are 4-byte aligned).  Loads into
+    // registers would stall the warp wherever the value is first moved or used.
+    uint32_t* ring = reinterpret_cast<uint32_t*>(smem + SK::kOffDt);
+    const uintptr_t dt_base = reinterpret_cast<uintptr_t>(p.dt);
+    auto dt_addr = [&](int64_t t) {       // byte address of token t's dt
+        return dt_base + 2 * (uintptr_t)(((int64_t)uc.b * p.L + t) * p.H + uc.h);
+    };
+    auto issue_dt = [&](int k) {
+        if (k < it.k1) {
+            const int64_t t = (int64_t)k * kTile + 4 * lane;
+            uint32_t* dst = ring + (k % SK::kDtRing) * kTile + 4 * lane;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (t + i < p.L) cp_async4(dst + i, reinterpret_cast<const void*>(dt_addr(t + i) & ~(uintptr_t)3));
+                else dst[i] = 0u;
+            }
+        }
+        cp_async_commit();   // one group per tile, empty past the piece's end
+    };
+    auto read_dt = [&](int k, float (&d)[4]) {
         const int64_t t = (int64_t)k * kTile + 4 * lane;
-        const unsigned short* src = reinterpret_cast<const unsigned short*>(p.dt) +
-                                    ((int64_t)uc.b * p.L + t) * p.H + uc.h;
+        const uint32_t* src = ring + (k % SK::kDtRing) * kTile + 4 * lane;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            r[i] = 0u;
-            if (t + i < p.L) r[i] = src[(int64_t)i * p.H];
+            const uint32_t v = src[i];
+            const bool hi = (dt_addr(t + i) & 2) != 0;
+            d[i] = __uint_as_float((hi ? (v >> 16) : (v & 0xffffu)) << 16);
         }
     };
-    auto to_f32 = [](const uint32_t (&r)[4], float (&d)[4]) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) d[i] = __uint_as_float(r[i] << 16);
-    };
-    // dt two tiles ahead: the grouping looks at the next tile's, which is then in registers
     const int n = it.k1 - it.k0;
-    uint32_t rcur[4], rnext[4] = {0u, 0u, 0u, 0u}, rnext2[4] = {0u, 0u, 0u, 0u};
-    load_dt(it.k0, rcur);
-    if (n > 1) load_dt(it.k0 + 1, rnext);
+#pragma unroll 1
+    for (int q = 0; q < SK::kDtAhead; ++q) issue_dt(it.k0 + q);
     int nmode = 0;            // the next tile: 0 per-tile update, 1 new group, 2 joins
     float goff = 0.f;         // the group's log2 decay before the current tile
     // each tile's cumsum is scanned once, as the previous iteration's look at the next tile
     float dcur[4], c2cur[4], clcur, dmxcur;
-    to_f32(rcur, dcur);
-    clcur = tile_scan2(dcur, A2, lane, c2cur);
+    cp_async_wait<SK::kDtAhead - 1>();
+    read_dt(it.k0, dcur);
+    clcur = tile_scan2f(dcur, A2, lane, c2cur);
     dmxcur = tile_dtmax(dcur);
     int j = 0;
     for (; j < n; ++j) {
         const int k = it.k0 + j, s = j % SK::kStages;
         const bool has1 = j + 1 < n;
-        if (j + 2 < n) load_dt(k + 2, rnext2);
+        issue_dt(k + SK::kDtAhead);   // the ring slot of tile k - (ring - ahead) is free
+        SSD_ST_TRACE_POINT(0, j);
         if (!sp_wait(&b.empty[s], ((uint32_t)(j / SK::kStages) & 1u) ^ 1u, b, p)) break;
+        SSD_ST_TRACE_POINT(1, j);
         uint8_t* st = smem + SK::kOffStage + s * SK::kStageBytes;
         if (lane == 0) {
             mbar_arrive_expect_tx(&b.full[s], SK::kStageBytes);
@@ -160,8 +205,9 @@ __device__ __forceinline__ void sp_producer(const Item& it, const UnitCoords& uc
         bool last = true;
         float dn[4], c2n[4], cln = 0.f, dmxn = 0.f;
         if (has1) {
-            to_f32(rnext, dn);
-            cln = tile_scan2(dn, A2, lane, c2n);
+            cp_async_wait<SK::kDtAhead - 1>();   // tile k + 1 has landed
+            read_dt(k + 1, dn);
+            cln = tile_scan2f(dn, A2, lane, c2n);
             dmxn = tile_dtmax(dn);
             nmode = !(cln >= -kGroupRange2 && dmxn <= kGroupDtMax)      ? 0
                     : (grouped && goff + clcur + cln >= -kGroupRange2)  ? 2
@@ -173,6 +219,7 @@ __device__ __forceinline__ void sp_producer(const Item& it, const UnitCoords& uc
                       (first ? 1 : 0) | (last ? 2 : 0));
         if (grouped) goff += clcur;
         mbar_arrive(&b.full[s]);
+        SSD_ST_TRACE_POINT(2, j);
         if (has1) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -182,11 +229,8 @@ __device__ __forceinline__ void sp_producer(const Item& it, const UnitCoords& uc
             clcur = cln;
             dmxcur = dmxn;
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            rnext[i] = rnext2[i];
-        }
     }
+    cp_async_wait<0>();
     if (st_abort_set(b) && lane == 0) {
         // the loads of every tile this loop issued must land before the CTA exits
         for (int q = j - SK::kStages; q < j; ++q)
@@ -205,7 +249,9 @@ __device__ __forceinline__ void sp_mma(const Item& it, StBars& b, const TcParams
     int g = -1;               // group of the current tile
     for (int j = 0; j < n; ++j) {
         const int s = j % SK::kStages, xb = j & 1;
+        SSD_ST_TRACE_POINT(3, j);
         if (!sp_wait(&b.xs_full[xb], (uint32_t)(j >> 1) & 1u, b, p)) break;
+        SSD_ST_TRACE_POINT(4, j);
         if (!sp_wait(&b.full[s], (uint32_t)(j / SK::kStages) & 1u, b, p)) break;
         const int fl = slots[s].sflags;
         if (fl & 1) {
@@ -221,6 +267,7 @@ __device__ __forceinline__ void sp_mma(const Item& it, StBars& b, const TcParams
         mma_commit_e(&b.xs_empty[xb]);
         mma_commit_e(&b.empty[s]);
         if (fl & 2) mma_commit_e(&b.s_full);
+        SSD_ST_TRACE_POINT(5, j);
     }
     // every MMA issued above has completed once this barrier's phase 0 completes
     mma_commit_e(&b.done);
@@ -253,8 +300,11 @@ __device__ __forceinline__ bool sp_compute(const Item& it, const UnitCoords& uc,
     const int n = it.k1 - it.k0;
     for (int j = 0; j < n; ++j) {
         const int s = j % SK::kStages, xb = j & 1;
+        SSD_ST_TRACE_POINT(6, j);
         if (!sp_wait(&b.full[s], (uint32_t)(j / SK::kStages) & 1u, b, p)) return false;
+        SSD_ST_TRACE_POINT(7, j);
         if (!sp_wait(&b.xs_empty[xb], ((uint32_t)(j >> 1) & 1u) ^ 1u, b, p)) return false;
+        SSD_ST_TRACE_POINT(8, j);
         // every field of the slot is read before xs_full: after it the MMA may complete and
         // the producer refill the stage
         const StSlot& sl = slots[s];
@@ -275,6 +325,7 @@ __device__ __forceinline__ bool sp_compute(const Item& it, const UnitCoords& uc,
         }
         fence_proxy_async_smem();
         mbar_arrive(&b.xs_full[xb]);
+        SSD_ST_TRACE_POINT(9, j);
         logd += clast2;
         if (fl & 2) {
             ++g;
