@@ -68,7 +68,8 @@ def load_peaks():
 
 # Source files each profiled kernel is built from (a traffic record is valid for these bytes).
 KERNEL_SOURCES = {
-    "ssd_tc128_kernel": ("tc128.cu", "tc_common.cuh", "tc_plan.cuh", "tc_ptx.cuh", "common.cuh"),
+    "ssd_tc128_kernel": ("tc128.cu", "tc_state.cuh", "tc_common.cuh", "tc_plan.cuh", "tc_ptx.cuh",
+                         "common.cuh"),
     "ssd_tc_kernel": ("tc.cu", "tc_common.cuh", "tc_plan.cuh", "tc_ptx.cuh", "common.cuh"),
     "step_kernel_vec": ("step.cu", "common.cuh"),
     "conv_staged_kernel": ("block_staged.cu", "block_math.cuh", "tc_common.cuh", "tc_ptx.cuh",
@@ -807,7 +808,9 @@ def measure_scan(args, w, dev, ws, rank, local):
         raise SystemExit(f"workload not supported: {m.ssd_scan_strerror(-path)}")
     wsb = m.ssd_scan_workspace_bytes(dims, w.chunk, path)
     workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    launches_per_call = {m.SSD_PATH_CHUNKED: 3, m.SSD_PATH_TC: 1}[path]
+    launches_per_call = m.ssd_scan_kernels_per_call(dims, w.chunk, path)
+    if launches_per_call <= 0:
+        raise SystemExit(f"kernel count: {m.ssd_scan_strerror(-launches_per_call)}")
 
     def step(i):
         d = sets[i % n_sets]

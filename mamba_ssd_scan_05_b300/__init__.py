@@ -28,6 +28,7 @@ from ._binding import (  # noqa: F401
     ssd_scan_gated_workspace_bytes,
     ssd_scan_get_status,
     ssd_scan_host_arena_bytes,
+    ssd_scan_kernels_per_call,
     ssd_scan_resolve_path,
     ssd_scan_set_wait_cycles,
     ssd_block_get_status,

@@ -54,6 +54,8 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_scan_resolve_path.restype = i32
         lib.ssd_scan_workspace_bytes.argtypes = [dims_p, i32, i32]
         lib.ssd_scan_workspace_bytes.restype = sz
+        lib.ssd_scan_kernels_per_call.argtypes = [dims_p, i32, i32]
+        lib.ssd_scan_kernels_per_call.restype = i32
         fwd_args = [dims_p, vp, vp, fp, vp, vp, fp, fp, i32, vp, fp, vp, sz, vp]
         lib.ssd_scan_fwd.argtypes = fwd_args
         lib.ssd_scan_fwd.restype = i32
@@ -133,6 +135,11 @@ def ssd_scan_resolve_path(dims: ssd_dims, chunk_size: int, path: int = SSD_PATH_
 
 def ssd_scan_workspace_bytes(dims: ssd_dims, chunk_size: int, path: int = SSD_PATH_AUTO) -> int:
     return load_library().ssd_scan_workspace_bytes(ctypes.byref(dims), int(chunk_size), int(path))
+
+
+def ssd_scan_kernels_per_call(dims: ssd_dims, chunk_size: int, path: int = SSD_PATH_AUTO) -> int:
+    """Kernels one ssd_scan_fwd call enqueues on the current device (negative: an SSD_ERR_*)."""
+    return load_library().ssd_scan_kernels_per_call(ctypes.byref(dims), int(chunk_size), int(path))
 
 
 def _check_inputs(x, dt, A, B, C, D, initial_state):

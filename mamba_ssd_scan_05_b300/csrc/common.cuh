@@ -124,6 +124,13 @@ int norm_staged_launch(const NormArgs& a);
 // ssd_scan_set_wait_cycles).
 long long tc_wait_budget();
 int tc128_launch(const ScanArgs& a);
+// The d_state 128 grid on `nsm` SMs (capped at max_ctas when > 0) and its plan mode: 1 when
+// ranges are no longer than a chain, so the state-only passes run first as a kernel of their own.
+void tc128_grid(int64_t batch, int64_t L, int64_t H, int64_t P, int nsm, int max_ctas,
+                int* n_ctas, int* pass1_mode);
+// Kernels one ungated or gated d_state 128 call launches on the current device (1 or 2), or a
+// negative SSD_ERR_* code.
+int tc128_kernels_per_call(int64_t batch, int64_t L, int64_t H, int64_t P);
 // Whether the d_state 128 kernel fuses the gated RMSNorm for this headdim and group size.
 bool tc128_gated_supports(int64_t P, int group);
 size_t tc_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t P, int64_t N, int Q);

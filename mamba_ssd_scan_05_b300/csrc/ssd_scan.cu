@@ -201,6 +201,15 @@ size_t ssd_scan_workspace_bytes(const ssd_dims* dims, int chunk_size, int path) 
     return workspace_for(dims, chunk_size, r);
 }
 
+int ssd_scan_kernels_per_call(const ssd_dims* dims, int chunk_size, int path) {
+    const int r = resolve(dims, chunk_size, path);
+    if (r < 0) return r;
+    if (r == SSD_PATH_CHUNKED) return 3;   // chunk states, state passing, chunk outputs
+    if (dims->dstate == 128)
+        return tc128_kernels_per_call(dims->batch, dims->seqlen, dims->nheads, dims->headdim);
+    return 1;
+}
+
 int ssd_scan_fwd(const ssd_dims* dims, const void* x, const void* dt, const float* A,
                  const void* B, const void* C, const float* D, const float* initial_state,
                  int chunk_size, void* y, float* final_state, void* workspace,

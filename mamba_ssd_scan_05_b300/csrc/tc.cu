@@ -650,12 +650,20 @@ bool tc_supports(int32_t dtype, int64_t P, int64_t N, int Q) {
     return dtype == SSD_BF16 && P % kPS == 0 && (N == 128 || N == 256) && Q % 64 == 0;
 }
 
-size_t tc_workspace_bytes(int64_t, int64_t, int64_t, int64_t, int64_t N, int) {
-    return kWsHeaderBytes + flags_bytes() + slots_bytes(N);
+size_t tc_workspace_bytes(int64_t b, int64_t L, int64_t H, int64_t P, int64_t N, int) {
+    size_t bytes = kWsHeaderBytes + flags_bytes() + slots_bytes(N);
+    if (N == 128) {
+        // segment records of the separate state-only pass
+        const int64_t tiles = (L + kTile - 1) / kTile;
+        bytes += (size_t)seg_records(b * H * (P / kPS) * tiles, kMaxCtas) * kSegRecBytes;
+    }
+    return bytes;
 }
 
 size_t tc_workspace_bytes_ctas(int64_t N, int ctas) {
-    return kWsHeaderBytes + flags_bytes() + sizeof(float) * 2 * (size_t)ctas * kPS * (size_t)N;
+    size_t bytes = kWsHeaderBytes + flags_bytes() + sizeof(float) * 2 * (size_t)ctas * kPS * (size_t)N;
+    if (N == 128) bytes += (size_t)5 * ctas * kSegRecBytes;
+    return bytes;
 }
 
 int tc_launch(const ScanArgs& a) {

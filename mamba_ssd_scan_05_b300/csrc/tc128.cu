@@ -878,7 +878,13 @@ int launch128(const ScanArgs& a, const TcParams& p) {
         cudaSuccess)
         return SSD_ERR_CUDA;
     if (ext) {
-        const int rc = tc128_state_launch(tmX, tmB, p, a.stream);
+        // segment records after the hand-off slots, as many as the workspace holds
+        const size_t off = seg_offset(a.max_ctas > 0 ? a.max_ctas : kMaxCtas);
+        const int64_t recs = a.ws_bytes > off ? (int64_t)((a.ws_bytes - off) / kSegRecBytes) : 0;
+        StTable tab;
+        int n_segs = 0;
+        int rc = st_table(p, reinterpret_cast<float*>(a.ws + off), recs, &tab, &n_segs);
+        if (rc == SSD_OK && n_segs > 0) rc = tc128_state_launch(tmX, tmB, p, tab, n_segs, a.stream);
         if (rc != SSD_OK) return rc;
     }
     kernel<<<(unsigned)p.n_ctas, K::kThreads, smem, a.stream>>>(tmX, tmB, tmC, p);
@@ -886,6 +892,26 @@ int launch128(const ScanArgs& a, const TcParams& p) {
 }
 
 }  // namespace
+
+void tc128_grid(int64_t batch, int64_t L, int64_t H, int64_t P, int nsm, int max_ctas,
+                int* n_ctas, int* pass1_mode) {
+    const int64_t n_tiles = (L + kTile - 1) / kTile;
+    const int64_t total = batch * H * (P / kPS) * n_tiles;
+    int ctas = (int)std::min<int64_t>(std::min(nsm, kMaxCtas), total);
+    if (max_ctas > 0) ctas = std::min(ctas, max_ctas);
+    *n_ctas = ctas;
+    // Without a state-only pass, a range's head piece is published before its successor's
+    // tail piece is needed as long as every range is longer than a chain.
+    *pass1_mode = (total / ctas) > n_tiles ? 0 : 1;
+}
+
+int tc128_kernels_per_call(int64_t batch, int64_t L, int64_t H, int64_t P) {
+    const int nsm = sm_count();
+    if (nsm <= 0) return -SSD_ERR_CUDA;
+    int ctas = 0, mode = 0;
+    tc128_grid(batch, L, H, P, nsm, 0, &ctas, &mode);
+    return mode == 1 ? 2 : 1;   // the state-only pass kernel, then the scan
+}
 
 bool tc128_gated_supports(int64_t P, int group) {
     return P % kPS == 0 && (group == 8 || group == 16 || group == 32 || group == 64);
@@ -901,12 +927,7 @@ int tc128_launch(const ScanArgs& a) {
     p.n_ps = (int)(a.headdim / kPS);
     p.n_tiles = (int)((a.seqlen + kTile - 1) / kTile);
     p.n_units = a.batch * a.nheads * p.n_ps;
-    const int64_t total = p.n_units * p.n_tiles;
-    p.n_ctas = (int)std::min<int64_t>(std::min(nsm, kMaxCtas), total);
-    if (a.max_ctas > 0) p.n_ctas = std::min(p.n_ctas, a.max_ctas);
-    // Without a state-only pass, a range's head piece is published before its successor's
-    // tail piece is needed as long as every range is longer than a chain.
-    p.pass1_mode = (total / p.n_ctas) > p.n_tiles ? 0 : 1;
+    tc128_grid(a.batch, a.seqlen, a.nheads, a.headdim, nsm, a.max_ctas, &p.n_ctas, &p.pass1_mode);
     p.dt = static_cast<const __nv_bfloat16*>(a.dt);
     p.A = a.A; p.D = a.D; p.h0 = a.h0;
     p.y = static_cast<__nv_bfloat16*>(a.y);

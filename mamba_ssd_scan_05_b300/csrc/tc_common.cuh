@@ -729,6 +729,14 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
 size_t flags_bytes() { return align_up(sizeof(int) * kFlagsPerCta * kMaxCtas, 256); }
 size_t slots_bytes(int64_t N) { return sizeof(float) * 2 * (size_t)kMaxCtas * kPS * (size_t)N; }
 
+// Segment records of the d_state-128 state-only pass (plan::seg_records of them), after the
+// hand-off slots of a grid capped at `cap` CTAs: each a local state [64 x 128] (slot layout)
+// and its log2 decay, padded to 16 bytes.
+constexpr size_t kSegRecBytes = sizeof(float) * kPS * 128 + 16;
+size_t seg_offset(int cap) {
+    return kWsHeaderBytes + flags_bytes() + sizeof(float) * 2 * (size_t)cap * kPS * 128;
+}
+
 int sm_count() {
     static int cache[64] = {0};
     int dev = 0;

@@ -105,5 +105,70 @@ SSD_HD bool lookback_uses_aggregate(int64_t n_units, int n_tiles, int n_ctas, in
     return pass1_mode != 0 && (int64_t)jp * total / n_ctas > (int64_t)u * n_tiles;
 }
 
+// The work of the separate state-only pass (d_state 128): the pieces of the plan in mode 1
+// whose end state it publishes, each cut into nseg segments of about equal length; segment s
+// of a piece covers tiles k0 + s len / nseg .. k0 + (s + 1) len / nseg (len = k1 - k0).  The
+// segments of a piece cut into several keep their local states in records rec0 .. rec0 +
+// nseg - 1 of the workspace.
+struct StPiece {
+    int u, k0, k1;      // unit and tile range
+    int cta;            // the scan CTA whose slot and flags receive the state
+    int agg;            // 1: aggregate (middle piece), 0: inclusive state (head piece)
+    int seg0, nseg;     // segments seg0 .. seg0 + nseg - 1 (grid indices)
+    int rec0;           // first record (pieces with nseg > 1)
+};
+constexpr int kSegMinTiles = 32;
+
+// Records a problem of `total_tiles` tiles may use on a grid of at most `cap` CTAs: with the
+// segment length z chosen below, the cut pieces (longer than z) hold at most 2 t / z records,
+// t the state-only tiles (at most total_tiles), and at most 5 per CTA (4 from the length, one
+// more per piece).  Monotone in the problem size, so a part of a problem never needs more.
+SSD_HD int64_t seg_records(int64_t total_tiles, int cap) {
+    const int64_t a = 5 * (int64_t)cap, b = total_tiles / (kSegMinTiles / 2);
+    return a < b ? a : b;
+}
+
+// Fills pieces[0 .. *n_pieces) for a grid of n_ctas CTAs and returns the number of segments
+// (-1 if more than max_pieces pieces).  Segments are at least kSegMinTiles long, about 4 per CTA
+// in all, and long enough that the cut pieces use at most `recs` records (none: every piece
+// stays whole).
+inline int state_segments(int64_t n_units, int n_tiles, int n_ctas, int64_t recs,
+                          StPiece* pieces, int max_pieces, int* n_pieces) {
+    int np = 0;
+    int64_t t1 = 0;
+    for (int c = 0; c < n_ctas; ++c) {
+        const Plan pl = make_plan(n_units, n_tiles, n_ctas, 1, c);
+        for (int i = 0; i < pl.n_items; ++i) {
+            const Item it = plan_item(pl, i, n_tiles);
+            if (!it.pass1) continue;
+            if (np >= max_pieces) return -1;
+            pieces[np++] = StPiece{it.u, it.k0, it.k1, c, it.fin == kFinAgg ? 1 : 0, 0, 1, 0};
+            t1 += it.k1 - it.k0;
+        }
+    }
+    const int64_t per = 4 * (int64_t)n_ctas;
+    int64_t z = t1 / per + (t1 % per != 0);
+    if (z < kSegMinTiles) z = kSegMinTiles;
+    if (recs > 0) {
+        // a cut piece (len > z) has ceil(len / z) < 2 len / z segments
+        const int64_t zr = (2 * t1) / recs + ((2 * t1) % recs != 0);
+        if (zr > z) z = zr;
+    } else {
+        z = (int64_t)1 << 40;   // no records: every piece stays whole
+    }
+    int s = 0, r = 0;
+    for (int q = 0; q < np; ++q) {
+        const int64_t len = pieces[q].k1 - pieces[q].k0;
+        const int64_t n = (len + z - 1) / z;
+        pieces[q].nseg = n < 1 ? 1 : (int)n;
+        pieces[q].seg0 = s;
+        pieces[q].rec0 = r;
+        s += pieces[q].nseg;
+        if (pieces[q].nseg > 1) r += pieces[q].nseg;
+    }
+    *n_pieces = np;
+    return s;
+}
+
 }  // namespace plan
 }  // namespace ssd

@@ -17,8 +17,8 @@
 // exceeds the group range is a group of one with the per-tile weights 2^(clast - c_t) dt_t and
 // h = 2^clast h + S.
 //
-// Roles (384 threads): warp 0 loads x and B by TMA (lane 0) and computes the tile's weights and
-// grouping (all lanes); warp 1 issues the MMAs; warps 4-11 (two warpgroups of 32 headdim
+// Roles (384 threads): warp 0 loads x and B by TMA (lane 0); warp 1 issues the MMAs; warp 2
+// computes each tile's weights and grouping from dt; warps 4-11 (two warpgroups of 32 headdim
 // columns) scale x into Xs and keep the state, row n = 32 (warp % 4) + lane of S^T.
 // Every wait is bounded; on a timeout the CTA records SSD_ERR_TIMEOUT, drains its copies and
 // MMAs and publishes nothing (the scan kernel's look-back then times out too).
@@ -67,6 +67,7 @@ struct StBars {
     uint64_t s_full, s_empty, done;
     uint32_t tmem;
     int abort;
+    int tma_n, dt_n;          // tiles loaded / tiles whose weights arrived
 };
 static_assert(sizeof(StBars) <= 256, "barrier block");
 
@@ -112,130 +113,202 @@ __device__ __forceinline__ float tile_scan2f(const float (&d0)[4], float A2, int
         const float n = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += n;
     }
-    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0.f;
+    const float excl = incl - cs[3];
 #pragma unroll
     for (int i = 0; i < 4; ++i) c2[i] = excl + cs[i];
     return __shfl_sync(0xffffffffu, incl, 31);
 }
 
-// The CTA's state-only item under plan mode 1 (the piece whose state it must publish), if any.
-__device__ __forceinline__ bool pass1_item(const TcParams& p, Item& out) {
-    const Plan pl = plan::make_plan(p.n_units, p.n_tiles, p.n_ctas, 1, (int)blockIdx.x);
-    for (int i = 0; i < pl.n_items; ++i) {
-        const Item it = plan_item(pl, i, p.n_tiles);
-        if (it.pass1) {
-            out = it;
-            return true;
-        }
-    }
-    return false;
+// A tile's largest dt (warp-uniform) by one integer reduction: floats mapped to signed integers
+// in the same order (negative values with their magnitude bits flipped).
+__device__ __forceinline__ float tile_dtmax_r(const float (&d0)[4]) {
+    const float m = fmaxf(fmaxf(d0[0], d0[1]), fmaxf(d0[2], d0[3]));
+    int key = __float_as_int(m);
+    key = key >= 0 ? key : key ^ 0x7fffffff;
+    key = __reduce_max_sync(0xffffffffu, key);
+    return __int_as_float(key >= 0 ? key : key ^ 0x7fffffff);
 }
 
-// ---- warp 0: x and B tiles, weights and grouping --------------------------------------------
+// The pieces of plan mode 1 whose end state the state-only pass publishes, each cut into
+// segments of about equal length (one CTA each, so that the hardware's block scheduler
+// balances the work over SMs of unequal speed and pieces of unequal length).  A segment
+// computes its local state from zero into a record; the piece's last segment to finish (a
+// counter in the piece's flag words) combines the records in order, h = 2^C_s h + S_s from the
+// initial state (head piece) or zero (middle piece), and publishes.  A piece of one segment
+// starts from its own initial state and publishes directly.
+struct StTable {
+    int n_pieces;
+    float* seg;         // segment records (kSegRecBytes each) in the workspace
+    StPiece piece[kMaxCtas];
+};
 
-__device__ __forceinline__ void sp_producer(const Item& it, const UnitCoords& uc, StBars& b,
-                                            const TcParams& p, uint8_t* smem, StSlot* slots,
-                                            const CUtensorMap* tmX, const CUtensorMap* tmB,
-                                            int lane) {
+// ---- warp 0: x and B tiles by TMA ------------------------------------------------------------
+
+__device__ __forceinline__ void sp_load(const Item& it, const UnitCoords& uc, StBars& b,
+                                        const TcParams& p, uint8_t* smem,
+                                        const CUtensorMap* tmX, const CUtensorMap* tmB, int lane) {
+    const int n = it.k1 - it.k0;
+    for (int j = 0; j < n; ++j) {
+        const int k = it.k0 + j, s = j % SK::kStages;
+        if (!sp_wait(&b.empty[s], ((uint32_t)(j / SK::kStages) & 1u) ^ 1u, b, p)) break;
+        if (lane == 0) {
+            uint8_t* st = smem + SK::kOffStage + s * SK::kStageBytes;
+            mbar_arrive_expect_tx(&b.full[s], SK::kStageBytes);
+            tma_load_4d(st, tmX, &b.full[s], uc.ps * kPS, uc.h, k * kTile, uc.b);
+            for (int r = 0; r < SK::kNReg; ++r)
+                tma_load_4d(st + SK::kXBytes + r * kTileBytes, tmB, &b.full[s], r * 64, uc.g,
+                            k * kTile, uc.b);
+            b.tma_n = j + 1;   // tiles issued (read after the CTA's last barrier)
+        }
+    }
+}
+
+// A tile's weights (4 tokens per lane) and its slot's scalars, computed ahead of the slot wait:
+// per-tile mode 2^(clast - c_t) dt_t, then H = 2^clast H + S; grouped 2^-(goff + c_t) dt_t, and at
+// the group's last tile H = 2^u (H + S) with u = goff + clast (the group's log2 decay).
+struct StW {
+    float w[4];
+    float udec2, sigma, clast2;
+    int sflags;
+};
+__device__ __forceinline__ StW st_weights(const float (&d0)[4], const float (&c2)[4], float clast2,
+                                          bool grouped, float goff, int sflags) {
+    StW r;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        r.w[i] = (grouped ? ex2(-(goff + c2[i])) : ex2(clast2 - c2[i])) * d0[i];
+    r.clast2 = clast2;
+    r.sflags = sflags;
+    r.udec2 = grouped ? goff + clast2 : clast2;
+    r.sigma = grouped ? ex2(r.udec2) : 1.f;
+    return r;
+}
+__device__ __forceinline__ void st_store(StSlot& sl, const StW& r, int lane) {
+    *reinterpret_cast<float4*>(sl.w + 4 * lane) = make_float4(r.w[0], r.w[1], r.w[2], r.w[3]);
+    if (lane == 0) {
+        sl.udec2 = r.udec2;
+        sl.sigma = r.sigma;
+        sl.clast2 = r.clast2;
+        sl.sflags = r.sflags;
+    }
+}
+
+// ---- warp 2: each tile's weights and grouping, from dt ---------------------------------------
+
+__device__ __forceinline__ void sp_weights(const Item& it, const UnitCoords& uc, StBars& b,
+                                           const TcParams& p, uint8_t* smem, StSlot* slots,
+                                           int lane) {
     const float A2 = p.A[uc.h] * kLog2e;
     // dt of tile k, 4 consecutive tokens per lane, copied asynchronously (cp.async) into a ring
     // in shared memory kDtAhead tiles ahead: the aligned 4-byte word holding each token's bf16
     // value (it lies inside the tensor's allocation, whose bounds are 4-byte aligned).  Loads into
     // registers would stall the warp wherever the value is first moved or used.
     uint32_t* ring = reinterpret_cast<uint32_t*>(smem + SK::kOffDt);
-    const uintptr_t dt_base = reinterpret_cast<uintptr_t>(p.dt);
-    auto dt_addr = [&](int64_t t) {       // byte address of token t's dt
-        return dt_base + 2 * (uintptr_t)(((int64_t)uc.b * p.L + t) * p.H + uc.h);
-    };
+    // token t's dt at byte a0 + t * stride; which half of its word does not depend on the tile
+    // (a tile advances the address by 256 H bytes)
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p.dt) +
+                         2 * (uintptr_t)((int64_t)uc.b * p.L * p.H + uc.h);
+    const uintptr_t stride = 2 * (uintptr_t)p.H;
+    int hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        hi |= (int)(((a0 + (uintptr_t)(4 * lane + i) * stride) >> 1) & 1u) << i;
     auto issue_dt = [&](int k) {
         if (k < it.k1) {
             const int64_t t = (int64_t)k * kTile + 4 * lane;
             uint32_t* dst = ring + (k % SK::kDtRing) * kTile + 4 * lane;
+            uintptr_t a = a0 + (uintptr_t)t * stride;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (t + i < p.L) cp_async4(dst + i, reinterpret_cast<const void*>(dt_addr(t + i) & ~(uintptr_t)3));
+            for (int i = 0; i < 4; ++i, a += stride) {
+                if (t + i < p.L) cp_async4(dst + i, reinterpret_cast<const void*>(a & ~(uintptr_t)3));
                 else dst[i] = 0u;
             }
         }
         cp_async_commit();   // one group per tile, empty past the piece's end
     };
     auto read_dt = [&](int k, float (&d)[4]) {
-        const int64_t t = (int64_t)k * kTile + 4 * lane;
         const uint32_t* src = ring + (k % SK::kDtRing) * kTile + 4 * lane;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t v = src[i];
-            const bool hi = (dt_addr(t + i) & 2) != 0;
-            d[i] = __uint_as_float((hi ? (v >> 16) : (v & 0xffffu)) << 16);
+            d[i] = __uint_as_float((((hi >> i) & 1) ? (v >> 16) : (v & 0xffffu)) << 16);
         }
     };
     const int n = it.k1 - it.k0;
 #pragma unroll 1
     for (int q = 0; q < SK::kDtAhead; ++q) issue_dt(it.k0 + q);
-    int nmode = 0;            // the next tile: 0 per-tile update, 1 new group, 2 joins
-    float goff = 0.f;         // the group's log2 decay before the current tile
-    // each tile's cumsum is scanned once, as the previous iteration's look at the next tile
-    float dcur[4], c2cur[4], clcur, dmxcur;
-    cp_async_wait<SK::kDtAhead - 1>();
-    read_dt(it.k0, dcur);
-    clcur = tile_scan2f(dcur, A2, lane, c2cur);
-    dmxcur = tile_dtmax(dcur);
-    int j = 0;
-    for (; j < n; ++j) {
-        const int k = it.k0 + j, s = j % SK::kStages;
-        const bool has1 = j + 1 < n;
-        issue_dt(k + SK::kDtAhead);   // the ring slot of tile k - (ring - ahead) is free
+    auto groupable = [](float cl, float dmx) { return cl >= -kGroupRange2 && dmx <= kGroupDtMax; };
+    // Tiles go in pairs (j, j + 1): both the pair's next tiles are scanned together (independent
+    // shuffle chains), and both weights are computed before the slot waits; only the flag that
+    // ends a group needs the tile after.  Tile j's cumsum was scanned by the previous pair.
+    float dA[4], cA[4], clA, dmA;
+    cp_async_wait<SK::kDtAhead - 1>();   // tile k0 has landed
+    read_dt(it.k0, dA);
+    clA = tile_scan2f(dA, A2, lane, cA);
+    dmA = tile_dtmax_r(dA);
+    int mode = groupable(clA, dmA) ? 1 : 0;   // tile j: 0 per-tile update, 1 new group, 2 joins
+    float goff = 0.f;                         // the group's log2 decay before the current tile
+    for (int j = 0; j < n; j += 2) {
+        const int k = it.k0 + j;
+        const bool has1 = j + 1 < n, has2 = j + 2 < n;
+        issue_dt(k + SK::kDtAhead);
+        issue_dt(k + 1 + SK::kDtAhead);
+        cp_async_wait<SK::kDtAhead - 1>();   // tiles k + 1 and k + 2 have landed
+        float dB[4], cB[4], dC[4], cC[4];
+        read_dt(k + 1, dB);
+        read_dt(k + 2, dC);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {   // past the piece's end the ring holds stale words
+            dB[i] = has1 ? dB[i] : 0.f;
+            dC[i] = has2 ? dC[i] : 0.f;
+        }
+        const float clB = tile_scan2f(dB, A2, lane, cB);
+        const float clC = tile_scan2f(dC, A2, lane, cC);
+        const float dmB = tile_dtmax_r(dB), dmC = tile_dtmax_r(dC);
+        // tile j
+        const bool gA = mode != 0, fA = mode != 2;
+        if (fA) goff = 0.f;
+        const int modeB = !(has1 && groupable(clB, dmB))                  ? 0
+                          : (gA && goff + clA + clB >= -kGroupRange2)     ? 2
+                                                                          : 1;
+        const bool lA = !has1 || modeB != 2;
+        const StW wA = st_weights(dA, cA, clA, gA, goff, (fA ? 1 : 0) | (lA ? 2 : 0));
+        if (gA) goff += clA;
+        // tile j + 1
+        const bool gB = modeB != 0, fB = modeB != 2;
+        if (fB) goff = 0.f;
+        const int modeC = !(has2 && groupable(clC, dmC))                  ? 0
+                          : (gB && goff + clB + clC >= -kGroupRange2)     ? 2
+                                                                          : 1;
+        const bool lB = !has2 || modeC != 2;
+        const StW wB = st_weights(dB, cB, clB, gB, goff, (fB ? 1 : 0) | (lB ? 2 : 0));
+        if (gB) goff += clB;
+        mode = modeC;
+        const int sA = j % SK::kStages;
         SSD_ST_TRACE_POINT(0, j);
-        if (!sp_wait(&b.empty[s], ((uint32_t)(j / SK::kStages) & 1u) ^ 1u, b, p)) break;
+        if (!sp_wait(&b.empty[sA], ((uint32_t)(j / SK::kStages) & 1u) ^ 1u, b, p)) break;
         SSD_ST_TRACE_POINT(1, j);
-        uint8_t* st = smem + SK::kOffStage + s * SK::kStageBytes;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&b.full[s], SK::kStageBytes);
-            tma_load_4d(st, tmX, &b.full[s], uc.ps * kPS, uc.h, k * kTile, uc.b);
-            for (int r = 0; r < SK::kNReg; ++r)
-                tma_load_4d(st + SK::kXBytes + r * kTileBytes, tmB, &b.full[s], r * 64, uc.g,
-                            k * kTile, uc.b);
-        }
-        // grouping: this tile joins the current group unless it starts one (or is on its own)
-        int mode = nmode;
-        if (j == 0) mode = (clcur >= -kGroupRange2 && dmxcur <= kGroupDtMax) ? 1 : 0;
-        const bool grouped = mode != 0, first = mode != 2;
-        if (first) goff = 0.f;
-        bool last = true;
-        float dn[4], c2n[4], cln = 0.f, dmxn = 0.f;
-        if (has1) {
-            cp_async_wait<SK::kDtAhead - 1>();   // tile k + 1 has landed
-            read_dt(k + 1, dn);
-            cln = tile_scan2f(dn, A2, lane, c2n);
-            dmxn = tile_dtmax(dn);
-            nmode = !(cln >= -kGroupRange2 && dmxn <= kGroupDtMax)      ? 0
-                    : (grouped && goff + clcur + cln >= -kGroupRange2)  ? 2
-                                                                        : 1;
-            last = nmode != 2;
-        }
-        state_weights(slots[s].w, slots[s].udec2, slots[s].sigma, slots[s].clast2,
-                      slots[s].sflags, dcur, c2cur, clcur, lane, grouped, goff,
-                      (first ? 1 : 0) | (last ? 2 : 0));
-        if (grouped) goff += clcur;
-        mbar_arrive(&b.full[s]);
+        st_store(slots[sA], wA, lane);
+        mbar_arrive(&b.full[sA]);
+        if (lane == 0) b.dt_n = j + 1;   // tiles whose weights arrived
         SSD_ST_TRACE_POINT(2, j);
         if (has1) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                dcur[i] = dn[i];
-                c2cur[i] = c2n[i];
-            }
-            clcur = cln;
-            dmxcur = dmxn;
+            const int sB = (j + 1) % SK::kStages;
+            if (!sp_wait(&b.empty[sB], ((uint32_t)((j + 1) / SK::kStages) & 1u) ^ 1u, b, p)) break;
+            st_store(slots[sB], wB, lane);
+            mbar_arrive(&b.full[sB]);
+            if (lane == 0) b.dt_n = j + 2;
+            SSD_ST_TRACE_POINT(2, j + 1);
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            dA[i] = dC[i];
+            cA[i] = cC[i];
+        }
+        clA = clC;
+        dmA = dmC;
     }
     cp_async_wait<0>();
-    if (st_abort_set(b) && lane == 0) {
-        // the loads of every tile this loop issued must land before the CTA exits
-        for (int q = j - SK::kStages; q < j; ++q)
-            if (q >= 0) drain_wait(&b.full[q % SK::kStages], (uint32_t)(q / SK::kStages) & 1u, p.ws);
-    }
     __syncwarp();
 }
 
@@ -280,19 +353,16 @@ __device__ __forceinline__ void sp_mma(const Item& it, StBars& b, const TcParams
 // Thread: token row (and state row) r = 32 (warp % 4) + lane; headdim columns c0 .. c0 + 31 of
 // its warpgroup.  Returns false on a timeout or abort; else leaves its part of the published
 // state in the CTA's slot and the piece's log2 decay in *logd_out.
-__device__ __forceinline__ bool sp_compute(const Item& it, const UnitCoords& uc, StBars& b,
-                                           const TcParams& p, uint8_t* smem,
-                                           const StSlot* slots, uint32_t tmem, int cw, int lane,
+__device__ __forceinline__ bool sp_compute(const Item& it, StBars& b, const TcParams& p,
+                                           uint8_t* smem, const StSlot* slots, uint32_t tmem,
+                                           int cw, int lane, const float* h0, float* out,
                                            float* logd_out) {
     const int q = cw & 3, wg = cw >> 2;
     const int r = 32 * q + lane, c0 = 32 * wg;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    // entering state: the chain's initial state (head piece) or zero (middle piece); element
-    // (p, n) of a head's state at p * d_state + n
+    // entering state: h0 (the initial state of the unit's 64 headdim rows, element (p, n) at
+    // p * d_state + n), or zero
     float h[32];
-    const float* h0 = (it.init == kInitH0 && p.h0)
-                          ? p.h0 + ((int64_t)uc.bh * p.P + (int64_t)uc.ps * kPS) * 128
-                          : nullptr;
 #pragma unroll
     for (int i = 0; i < 32; ++i) h[i] = h0 ? h0[(c0 + i) * 128 + r] : 0.f;
     float logd = 0.f;
@@ -340,29 +410,89 @@ __device__ __forceinline__ bool sp_compute(const Item& it, const UnitCoords& uc,
             mbar_arrive(&b.s_empty);
         }
     }
-    // this thread's part of the publication, in the scan kernel's slot layout (element (p, n) at
-    // p * d_state + n of the CTA's inclusive or aggregate slot)
-    const int64_t slot_elems = (int64_t)kPS * 128;
-    float* slot = p.slots + (int64_t)blockIdx.x * 2 * slot_elems +
-                  (it.fin == kFinAgg ? slot_elems : 0);
+    // this thread's part of the state, in the scan kernel's slot layout (element (p, n) at
+    // p * d_state + n)
 #pragma unroll
-    for (int i = 0; i < 32; ++i) slot[(c0 + i) * 128 + r] = h[i];
+    for (int i = 0; i < 32; ++i) out[(c0 + i) * 128 + r] = h[i];
     __threadfence();
     *logd_out = logd;
     return true;
 }
 
+// The last segment of a multi-segment piece: combines the records of the piece's segments in
+// order into the scan's slot and returns the piece's log2 decay.  All threads; each owns
+// float4 columns tid, tid + kThreads, ... of the [64 x 128] state.
+__device__ __forceinline__ float st_combine(const StPiece& pc, const StTable& tab,
+                                            const float* h0, float* slot) {
+    constexpr int kE = kPS * 128, kE4 = kE / 4;
+    constexpr int kPer = (kE4 + SK::kThreads - 1) / SK::kThreads;
+    constexpr int kRec = (int)(kSegRecBytes / sizeof(float));
+    float4 h[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int e = 4 * ((int)threadIdx.x + k * SK::kThreads);
+        h[k] = (h0 && e < kE) ? make_float4(h0[e], h0[e + 1], h0[e + 2], h0[e + 3])
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float logd = 0.f;
+#pragma unroll 1
+    for (int q = 0; q < pc.nseg; ++q) {
+        const float* rec = tab.seg + (int64_t)(pc.rec0 + q) * kRec;
+        const float ls = __ldcg(rec + kE);
+        const float d = ex2(ls);
+        logd += ls;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int e4 = (int)threadIdx.x + k * SK::kThreads;
+            if (e4 < kE4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(rec) + e4);
+                h[k] = make_float4(fmaf(d, h[k].x, v.x), fmaf(d, h[k].y, v.y),
+                                   fmaf(d, h[k].z, v.z), fmaf(d, h[k].w, v.w));
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int e4 = (int)threadIdx.x + k * SK::kThreads;
+        if (e4 < kE4) reinterpret_cast<float4*>(slot)[e4] = h[k];
+    }
+    __threadfence();
+    return logd;
+}
+
 __global__ void __launch_bounds__(SK::kThreads, 1)
     ssd_state_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ TcParams p) {
+                     const __grid_constant__ TcParams p, const __grid_constant__ StTable tab) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     StBars& b = *reinterpret_cast<StBars*>(smem + SK::kOffBar);
     StSlot* slots = reinterpret_cast<StSlot*>(smem + SK::kOffSlot);
     __shared__ float logd_sh;
+    __shared__ int last_sh;
+    // this CTA's segment, of the last piece whose first segment is at most blockIdx.x
+    int c = 0;
+    for (int hi = tab.n_pieces - 1; c < hi;) {
+        const int mid = (c + hi + 1) >> 1;
+        if (tab.piece[mid].seg0 <= (int)blockIdx.x) c = mid;
+        else hi = mid - 1;
+    }
+    const StPiece& pc = tab.piece[c];
+    const int si = (int)blockIdx.x - pc.seg0, len = pc.k1 - pc.k0;
     Item it;
-    if (!pass1_item(p, it)) return;          // this CTA's range publishes nothing
+    it.u = pc.u;
+    it.k0 = pc.k0 + (int)((int64_t)si * len / pc.nseg);
+    it.k1 = pc.k0 + (int)((int64_t)(si + 1) * len / pc.nseg);
+    it.pass1 = 1;
+    it.init = kInitZero;
+    it.fin = kFinAgg;
     const UnitCoords uc = unit_coords(p, it.u);
+    const bool direct = pc.nseg == 1;
+    constexpr int64_t kE = (int64_t)kPS * 128;
+    float* slot = p.slots + (int64_t)pc.cta * 2 * kE + (pc.agg ? kE : 0);
+    float* rec = tab.seg + (int64_t)(pc.rec0 + si) * (int64_t)(kSegRecBytes / sizeof(float));
+    // the unit's initial state, where the piece (a head piece) starts from it
+    const float* h0 = (!pc.agg && p.h0) ? p.h0 + ((int64_t)uc.bh * p.P + (int64_t)uc.ps * kPS) * 128
+                                        : nullptr;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < SK::kStages; ++i) {
@@ -377,6 +507,8 @@ __global__ void __launch_bounds__(SK::kThreads, 1)
         mbar_init(&b.s_empty, SK::kCompute);
         mbar_init(&b.done, 1);
         b.abort = 0;
+        b.tma_n = 0;
+        b.dt_n = 0;
         fence_mbar_init();
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmB);
@@ -391,34 +523,73 @@ __global__ void __launch_bounds__(SK::kThreads, 1)
     const uint32_t tmem = b.tmem;
     bool ok = true;
     if (warp == 0) {
-        sp_producer(it, uc, b, p, smem, slots, &tmX, &tmB, lane);
+        sp_load(it, uc, b, p, smem, &tmX, &tmB, lane);
     } else if (warp == 1) {
         sp_mma(it, b, p, slots, smem_u32(smem), tmem, lane);
+    } else if (warp == 2) {
+        sp_weights(it, uc, b, p, smem, slots, lane);
     } else if (warp >= SK::kWarpC) {
         float logd = 0.f;
-        ok = sp_compute(it, uc, b, p, smem, slots, tmem, warp - SK::kWarpC, lane, &logd);
+        ok = sp_compute(it, b, p, smem, slots, tmem, warp - SK::kWarpC, lane,
+                        direct ? h0 : nullptr, direct ? slot : rec, &logd);
         if (warp == SK::kWarpC && lane == 0) logd_sh = logd;
     }
     ok = __syncthreads_and(ok) && !st_abort_set(b);
-    if (ok && threadIdx.x == 0) {
-        // every compute warp's part of the state is written: publish it for all 16 warps of
-        // the scan kernel (the aggregate's log2 decay first)
-        __threadfence();
-        for (int w = 0; w < 16; ++w) {
-            int* f = p.flags + (int)blockIdx.x * kFlagsPerCta + w * 4;
-            if (it.fin == kFinAgg) st_relaxed_gpu(f + 2, __float_as_int(logd_sh));
-            st_release_gpu(f + (it.fin == kFinAgg ? 1 : 0), 1);
+    if (!ok && threadIdx.x == 0) {
+        // after an abort the loads of the last tiles issued must land before the CTA exits.  A
+        // stage whose weights never arrived gets stand-in arrivals so that its phase can
+        // complete; the loads run at most kStages tiles ahead of the weights (a stage is
+        // refilled only after the MMA of its previous tile, which waited for that tile's weights).
+        const int nt = b.tma_n;
+        for (int q = b.dt_n; q < nt; ++q) mbar_arrive_cnt(&b.full[q % SK::kStages], 32);
+        for (int q = nt - SK::kStages; q < nt; ++q)
+            if (q >= 0) drain_wait(&b.full[q % SK::kStages], (uint32_t)(q / SK::kStages) & 1u, p.ws);
+    }
+    if (threadIdx.x == 0) {
+        // a multi-segment piece: the record's log2 decay, then the count of finished segments
+        // (release); the last one to finish (acquire) combines
+        int last = ok ? 1 : 0;
+        if (ok && !direct) {
+            rec[kE] = logd_sh;
+            __threadfence();
+            last = atomicAdd(p.flags + pc.cta * kFlagsPerCta + 3, 1) == pc.nseg - 1;
+            if (last) __threadfence();
         }
+        last_sh = last;
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, SK::kTmemCols);
+    if (!last_sh) return;
+    const float logd = direct ? logd_sh : st_combine(pc, tab, h0, slot);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // every thread's part of the state is written: publish it for all 16 warps of the scan
+        // kernel (the aggregate's log2 decay first)
+        __threadfence();
+        for (int w = 0; w < 16; ++w) {
+            int* f = p.flags + pc.cta * kFlagsPerCta + w * 4;
+            if (pc.agg) st_relaxed_gpu(f + 2, __float_as_int(logd));
+            st_release_gpu(f + (pc.agg ? 1 : 0), 1);
+        }
+    }
 }
 
-// The state-only pass of the d_state-128 scan for the CTAs of plan `p` (launched before the
-// scan kernel, which then runs in plan mode 2).  tmX / tmB are the scan's tensor maps.
+// Host: the table of the state-only pass, its segments within the `recs` records of `seg`.
+inline int st_table(const TcParams& p, float* seg, int64_t recs, StTable* tab, int* n_segs) {
+    const int s = state_segments(p.n_units, p.n_tiles, p.n_ctas, recs, tab->piece, kMaxCtas,
+                                 &tab->n_pieces);
+    if (s < 0) return SSD_ERR_UNSUPPORTED;
+    tab->seg = seg;
+    *n_segs = s;
+    return SSD_OK;
+}
+
+// The state-only pass of the d_state-128 scan for plan `p` (launched before the scan kernel,
+// whose plan then leaves these items out): one CTA per segment of `tab`.  tmX / tmB are the
+// scan's tensor maps.
 int tc128_state_launch(const CUtensorMap& tmX, const CUtensorMap& tmB, const TcParams& p,
-                       cudaStream_t st) {
+                       const StTable& tab, int n_segs, cudaStream_t st) {
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(ssd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -426,7 +597,7 @@ int tc128_state_launch(const CUtensorMap& tmX, const CUtensorMap& tmB, const TcP
             return SSD_ERR_CUDA;
         attr = true;
     }
-    ssd_state_kernel<<<(unsigned)p.n_ctas, SK::kThreads, SK::kSmem, st>>>(tmX, tmB, p);
+    ssd_state_kernel<<<(unsigned)n_segs, SK::kThreads, SK::kSmem, st>>>(tmX, tmB, p, tab);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -10,7 +10,12 @@
 //   4. a CTA publishes for one chain only (its flags are per CTA), at most one inclusive state
 //      and one aggregate;
 //   5. every chain ends in exactly one final-state item, at its last tile;
-//   6. a state-only pass covers the same tiles as the piece it precedes.
+//   6. a state-only pass covers the same tiles as the piece it precedes;
+//   7. the separate state-only pass's segments (state_segments): its pieces are exactly the
+//      state-only items of mode 1, each cut into non-empty segments that tile it in order,
+//      with contiguous grid indices; the segments of cut pieces take consecutive records and
+//      fit the records the workspace holds (the count it reserves, or fewer), segments of a
+//      cut piece are at least half the minimum length, and there are at most 5 per CTA.
 // Prints the first violations and exits non-zero if there are any.
 #include <cstdio>
 #include <cstdlib>
@@ -157,6 +162,62 @@ void check(long U, int T, int C, int p1) {
     }
 }
 
+// 7: segments for a grid of C CTAs with `recs` records in the workspace
+void check_segments(long U, int T, int C, long recs) {
+    std::vector<StPiece> pieces(256);
+    int np = 0;
+    const int s = state_segments(U, T, C, recs, pieces.data(), 256, &np);
+    if (s < 0) {
+        fail("segments: too many pieces", U, T, C, 2, -1, recs);
+        return;
+    }
+    // the pieces are the state-only items of mode 1, in CTA order
+    int q = 0;
+    for (int c = 0; c < C; ++c) {
+        const Plan pl = make_plan(U, T, C, 1, c);
+        for (int i = 0; i < pl.n_items; ++i) {
+            const Item it = plan_item(pl, i, T);
+            if (!it.pass1) continue;
+            if (q >= np) {
+                fail("segments: a state-only item without a piece", U, T, C, 2, c, i);
+                return;
+            }
+            const StPiece& pc = pieces[(size_t)q++];
+            if (pc.u != it.u || pc.k0 != it.k0 || pc.k1 != it.k1 || pc.cta != c ||
+                pc.agg != (it.fin == kFinAgg ? 1 : 0))
+                fail("segments: piece differs from its state-only item", U, T, C, 2, c, i);
+        }
+    }
+    if (q != np) fail("segments: extra pieces", U, T, C, 2, -1, np - q);
+    int next = 0, rec = 0;
+    long cut = 0;
+    for (int i = 0; i < np; ++i) {
+        const StPiece& pc = pieces[(size_t)i];
+        const int len = pc.k1 - pc.k0;
+        if (pc.seg0 != next || pc.nseg < 1 || pc.nseg > len)
+            fail("segments: indices or count", U, T, C, 2, pc.cta, pc.nseg);
+        int pos = pc.k0;
+        for (int g = 0; g < pc.nseg; ++g) {
+            const int a = pc.k0 + (int)((long)g * len / pc.nseg);
+            const int b = pc.k0 + (int)((long)(g + 1) * len / pc.nseg);
+            if (a != pos || b <= a) fail("segments: do not tile the piece", U, T, C, 2, pc.cta, g);
+            if (pc.nseg > 1 && b - a < kSegMinTiles / 2)
+                fail("segments: too short", U, T, C, 2, pc.cta, b - a);
+            pos = b;
+        }
+        if (pos != pc.k1) fail("segments: piece not covered", U, T, C, 2, pc.cta, pos);
+        if (pc.nseg > 1) {
+            if (pc.rec0 != rec) fail("segments: record indices", U, T, C, 2, pc.cta, pc.rec0);
+            rec += pc.nseg;
+            cut += pc.nseg;
+        }
+        next += pc.nseg;
+    }
+    if (next != s) fail("segments: count returned", U, T, C, 2, -1, s);
+    if (cut > recs) fail("segments: records overflow", U, T, C, 2, -1, cut);
+    if (s > 5L * C) fail("segments: more than 5 per CTA", U, T, C, 2, -1, s);
+}
+
 }  // namespace
 
 int main() {
@@ -173,6 +234,10 @@ int main() {
                     check(U, T, C, p1);
                     ++cases;
                 }
+                // the records a workspace reserves for C CTAs (5 per CTA, fewer for short
+                // problems), none, as many as pieces, and one more
+                for (long recs : {(long)seg_records(total, C), 0L, 1L, 7L, (long)C, 100000L})
+                    check_segments(U, T, C, recs);
             }
     std::printf("%ld plans checked, %d violations\n", cases, g_fail);
     return g_fail ? 1 : 0;

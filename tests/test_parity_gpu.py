@@ -159,8 +159,10 @@ def test_gpu_sequence_split_matches_one_call():
 
 # b, L, H, P, N, G, dtype, Q: pieces of batch rows (2 and 3 rows, uneven groups), pieces of
 # 256 tokens with the state carried (eight, the last one ragged; one short sequence), the
-# float32 chunked path
+# float32 chunked path; and rows of 80 heads, whose pieces need the separate state-only pass
+# while the whole problem does not (so the arena holds no segment records for it)
 HOST_CASES = [
+    (4, 512, 80, 64, 128, 1, "bf16", 256),
     (2, 400, 4, 64, 128, 2, "bf16", 128),
     (3, 300, 2, 64, 128, 1, "bf16", 64),
     (1, 2000, 4, 64, 128, 1, "bf16", 256),

@@ -35,6 +35,11 @@ MUTANTS = {
     "tail_no_look_back": ("return Item{pl.u0, pl.k0, (pl.u0 == pl.u1) ? pl.k1 : T, 0, kInitLookback, kFinFinal};",
                           "return Item{pl.u0, pl.k0, (pl.u0 == pl.u1) ? pl.k1 : T, 0, kInitH0, kFinFinal};"),
     # the look-back rule taking an aggregate also from the head piece's CTA
+    # segments taken half as long as they may be (more records than the workspace holds)
+    "segments_overflow": ("const int64_t zr = (2 * t1) / recs + ((2 * t1) % recs != 0);",
+                          "const int64_t zr = t1 / recs + (t1 % recs != 0);"),
+    # the next piece's segments starting one grid index too early (two CTAs on one segment)
+    "segments_index": ("        s += pieces[q].nseg;", "        s += pieces[q].nseg - (pieces[q].nseg > 1);"),
     "lookback_rule": ("return pass1_mode != 0 && (int64_t)jp * total / n_ctas > (int64_t)u * n_tiles;",
                       "return pass1_mode != 0 && (int64_t)jp * total / n_ctas >= (int64_t)u * n_tiles;"),
 }
