@@ -86,8 +86,10 @@ int ssd_scan_resolve_path(const ssd_dims* dims, int chunk_size, int path);
 
 /* Device workspace bytes ssd_scan_fwd needs for this problem and path (0 on invalid input).
  * The workspace holds a status word, per-chunk float32 states for the chunked path, and the
- * cross-block state hand-off slots of the tensor-core path.  Its contents need no
- * initialisation; calls sharing one workspace must be ordered on one stream. */
+ * cross-block state hand-off slots of the tensor-core path; for d_state 128 also the segment
+ * records of its state-only pass (long sequences over few heads: ranges of tiles shorter than
+ * the chains), which balance that pass over the SMs.  Its contents need no initialisation;
+ * calls sharing one workspace must be ordered on one stream. */
 size_t ssd_scan_workspace_bytes(const ssd_dims* dims, int chunk_size, int path);
 
 /* How many kernels one ssd_scan_fwd (or ssd_scan_fwd_gated) call enqueues for this problem on

@@ -910,7 +910,14 @@ int tc128_kernels_per_call(int64_t batch, int64_t L, int64_t H, int64_t P) {
     if (nsm <= 0) return -SSD_ERR_CUDA;
     int ctas = 0, mode = 0;
     tc128_grid(batch, L, H, P, nsm, 0, &ctas, &mode);
-    return mode == 1 ? 2 : 1;   // the state-only pass kernel, then the scan
+    if (mode != 1) return 1;
+    // the state-only pass kernel runs when some range ends inside a chain
+    static thread_local plan::StPiece pieces[kMaxCtas];
+    int np = 0;
+    const int64_t n_tiles = (L + kTile - 1) / kTile;
+    if (plan::state_segments(batch * H * (P / kPS), (int)n_tiles, ctas, 0, pieces, kMaxCtas, &np) < 0)
+        return -SSD_ERR_UNSUPPORTED;
+    return np > 0 ? 2 : 1;
 }
 
 bool tc128_gated_supports(int64_t P, int group) {

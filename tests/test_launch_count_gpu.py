@@ -33,9 +33,19 @@ def _kernel_events(fn):
     return [n for n in names if "memset" not in n.lower() and "memcpy" not in n.lower()]
 
 
-@pytest.mark.parametrize("case", CASES, ids=["tc128-pieces", "tc128-many-heads", "tc256",
-                                             "chunked"])
+def _aligned_case():
+    # as many heads as SMs: every CTA's range is one whole chain, so nothing is published and
+    # the state-only pass does not run although the plan is in its mode
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    return ((1, 1024, nsm, 64, 128, 1, 256, "bf16"), SSD_PATH_TC, 1)
+
+
+@pytest.mark.parametrize("case", CASES + ["aligned"],
+                         ids=["tc128-pieces", "tc128-many-heads", "tc256", "chunked",
+                              "tc128-ranges-are-chains"])
 def test_kernels_per_call_matches_profiler(case):
+    if case == "aligned":
+        case = _aligned_case()
     (b, L, H, P, N, G, Q, dt), path, expected = case
     inp = workloads.make_shape_inputs(b, L, H, P, N, G, dt, seed=5, h0_mode="normal",
                                       d_mode="normal")
