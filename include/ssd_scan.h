@@ -129,11 +129,12 @@ int ssd_scan_fwd_path(const ssd_dims* dims,
  * Host-buffer variant: every tensor argument is a HOST pointer (page-locked memory makes the
  * copies asynchronous), and `device_arena` is a caller-owned device buffer of at least
  * ssd_scan_host_arena_bytes(dims, chunk_size) bytes (256-byte aligned).  The problem is cut
- * into up to 8 pieces -- groups of batch rows, or (batch 1) stretches of multiples of 256
- * tokens with the state carried on the device -- and each piece's copies in, scan and copies
- * out form a pipeline: the copies run on two library-owned streams of the current device
- * (created on first use), ordered against `stream` with events, so piece p's inputs travel
- * while piece p - 1 is scanned and piece p - 2's outputs come back.  `stream` itself waits
+ * into up to 8 pieces -- groups of batch rows when there are 8 rows or more, else each row cut
+ * into 8 / batch stretches of multiples of 256 tokens with the row's state carried on the
+ * device -- and each piece's copies in, scan and copies out form a pipeline: the copies run on
+ * two library-owned streams of the current device (created on first use), ordered against
+ * `stream` with events, so piece p's inputs travel while piece p - 1 is scanned and earlier
+ * pieces' outputs come back.  `stream` itself waits
  * for every copy: the host outputs are valid after the caller synchronises `stream`.  Calls
  * enqueue under a process-wide lock.  The status word (ssd_scan_get_status on the arena's
  * workspace part) covers the whole call.  Same errors as ssd_scan_fwd.

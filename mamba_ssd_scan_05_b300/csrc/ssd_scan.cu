@@ -262,16 +262,20 @@ int ssd_scan_fwd_host(const ssd_dims* dims, const void* x, const void* dt, const
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
 
-    // Pieces: groups of batch rows (independent problems) when there are several rows, else
-    // stretches of the sequence whose state is carried on the device (multiples of 256 tokens,
-    // so each piece boundary is also a chunk and tile boundary).  Piece p's copies in run on
-    // the copy-in stream while piece p - 1 scans on `stream` and piece p - 2's outputs go back
-    // on the copy-out stream.
+    // Pieces: with at least kHostPieces rows, groups of batch rows (independent problems); with
+    // fewer, each row cut into kHostPieces / b stretches of the sequence whose state is carried
+    // on the device (multiples of 256 tokens, so each piece boundary is also a chunk and tile
+    // boundary).  Piece p's copies in run on the copy-in stream while piece p - 1 scans on
+    // `stream` and earlier pieces' outputs go back on the copy-out stream; more pieces leave
+    // less of the first copy in and the last copy out without overlap.
     const int64_t b = dims->batch, L = dims->seqlen;
-    const bool by_rows = b > 1;
-    const int64_t span = by_rows ? b : (L + 255) / 256;              // rows, or 256-token blocks
-    const int np = (int)std::max<int64_t>(1, std::min<int64_t>(kHostPieces, span));
-    auto piece_lo = [&](int i) { return span * i / np; };
+    const int64_t blocks = (L + 255) / 256;                           // 256-token blocks
+    const int ns = (int)std::max<int64_t>(1, std::min<int64_t>(kHostPieces / std::max<int64_t>(b, 1), blocks));
+    const bool by_rows = ns == 1;
+    const int ngr = by_rows ? (int)std::max<int64_t>(1, std::min<int64_t>(kHostPieces, b)) : (int)b;
+    const int np = ngr * ns;
+    auto row_lo = [&](int g) { return b * g / ngr; };                // row group g's first row
+    auto tok_lo = [&](int j) { return std::min<int64_t>(256 * (blocks * j / ns), L); };
     // per-token / per-row byte strides of each tensor
     const size_t eb = elem_bytes(dims->dtype);
     const size_t x_tok = eb * (size_t)(dims->nheads * dims->headdim);
@@ -295,21 +299,17 @@ int ssd_scan_fwd_host(const ssd_dims* dims, const void* x, const void* dt, const
     if (D) chk(cudaMemcpyAsync(dD, D, s.D, h2d, hp->in));
     if (initial_state) chk(cudaMemcpyAsync(dh0, initial_state, s.st, h2d, hp->in));
     for (int i = 0; i < np && ok && rc == SSD_OK; ++i) {
-        const int64_t lo = piece_lo(i), hi = piece_lo(i + 1);
+        // rows lo .. hi - 1, tokens t0 .. t1 - 1 (one row when the rows are cut into stretches)
+        const int g = i / ns, j = i % ns;
+        const int64_t lo = by_rows ? row_lo(g) : g, hi = by_rows ? row_lo(g + 1) : g + 1;
+        const int64_t t0 = tok_lo(j), t1 = tok_lo(j + 1);
         ssd_dims pd = *dims;
-        size_t ox, odt, obc, n_x, n_dt, n_bc;   // byte offsets and sizes of the piece
-        if (by_rows) {
-            pd.batch = hi - lo;
-            ox = x_tok * (size_t)(lo * L);       n_x = x_tok * (size_t)(pd.batch * L);
-            odt = dt_tok * (size_t)(lo * L);     n_dt = dt_tok * (size_t)(pd.batch * L);
-            obc = bc_tok * (size_t)(lo * L);     n_bc = bc_tok * (size_t)(pd.batch * L);
-        } else {
-            const int64_t t0 = lo * 256, t1 = std::min<int64_t>(hi * 256, L);
-            pd.seqlen = t1 - t0;
-            ox = x_tok * (size_t)t0;             n_x = x_tok * (size_t)pd.seqlen;
-            odt = dt_tok * (size_t)t0;           n_dt = dt_tok * (size_t)pd.seqlen;
-            obc = bc_tok * (size_t)t0;           n_bc = bc_tok * (size_t)pd.seqlen;
-        }
+        pd.batch = hi - lo;
+        pd.seqlen = t1 - t0;
+        const int64_t tok0 = lo * L + t0, ntok = pd.batch * pd.seqlen;   // contiguous tokens
+        const size_t ox = x_tok * (size_t)tok0, n_x = x_tok * (size_t)ntok;
+        const size_t odt = dt_tok * (size_t)tok0, n_dt = dt_tok * (size_t)ntok;
+        const size_t obc = bc_tok * (size_t)tok0, n_bc = bc_tok * (size_t)ntok;
         const auto* cx = static_cast<const uint8_t*>(x);
         const auto* cdt = static_cast<const uint8_t*>(dt);
         const auto* cB = static_cast<const uint8_t*>(B);
@@ -321,17 +321,18 @@ int ssd_scan_fwd_host(const ssd_dims* dims, const void* x, const void* dt, const
         chk(cudaEventRecord(hp->in_done[i], hp->in));
         chk(cudaStreamWaitEvent(st, hp->in_done[i], 0));
         if (!ok) break;
-        // the piece's entering and final state: its rows of h0 / hT, or (sequence pieces) the
-        // running state, which alternates between the two state buffers
+        // the piece's entering and final state: its rows of h0 / hT, or (stretches of a row)
+        // the row's running state, which alternates between its slices of the two buffers
+        const size_t so = st_row / sizeof(float) * (size_t)lo;
         const float* h_in;
         float* h_out;
         if (by_rows) {
-            h_in = initial_state ? dh0 + st_row / sizeof(float) * (size_t)lo : nullptr;
-            h_out = final_state ? dhT + st_row / sizeof(float) * (size_t)lo : nullptr;
+            h_in = initial_state ? dh0 + so : nullptr;
+            h_out = final_state ? dhT + so : nullptr;
         } else {
-            h_in = i == 0 ? (initial_state ? dh0 : nullptr) : ((i & 1) ? dhT : dh0);
-            h_out = (np == 1 || i == np - 1) ? (final_state ? ((i & 1) ? dh0 : dhT) : nullptr)
-                                              : ((i & 1) ? dh0 : dhT);
+            h_in = j == 0 ? (initial_state ? dh0 + so : nullptr) : ((j & 1) ? dhT : dh0) + so;
+            h_out = j == ns - 1 ? (final_state ? ((j & 1) ? dh0 : dhT) + so : nullptr)
+                                : ((j & 1) ? dh0 : dhT) + so;
         }
         rc = run(&pd, dx + ox, ddt + odt, dA, dB + obc, dC + obc, D ? dD : nullptr, h_in,
                  chunk_size, dy + ox, h_out, dws, ws_bytes, stream, SSD_PATH_AUTO,
@@ -341,11 +342,11 @@ int ssd_scan_fwd_host(const ssd_dims* dims, const void* x, const void* dt, const
         chk(cudaStreamWaitEvent(hp->out, hp->scan_done[i], 0));
         if (n_x) chk(cudaMemcpyAsync(static_cast<uint8_t*>(y) + ox, dy + ox, n_x, d2h, hp->out));
         if (by_rows && final_state)
-            chk(cudaMemcpyAsync(final_state + st_row / sizeof(float) * (size_t)lo,
-                                dhT + st_row / sizeof(float) * (size_t)lo,
-                                st_row * (size_t)pd.batch, d2h, hp->out));
-        if (!by_rows && final_state && i == np - 1)
-            chk(cudaMemcpyAsync(final_state, (i & 1) ? dh0 : dhT, s.st, d2h, hp->out));
+            chk(cudaMemcpyAsync(final_state + so, dhT + so, st_row * (size_t)pd.batch, d2h,
+                                hp->out));
+        if (!by_rows && final_state && j == ns - 1)
+            chk(cudaMemcpyAsync(final_state + so, ((j & 1) ? dh0 : dhT) + so, st_row, d2h,
+                                hp->out));
     }
     // `stream` ends after both copy streams: the caller's synchronisation covers every copy
     chk(cudaEventRecord(hp->join, hp->in));
