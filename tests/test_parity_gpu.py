@@ -195,3 +195,20 @@ def test_device_errors_raise():
         ssd_scan_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], chunk_size=0)
     with pytest.raises(TypeError):
         ssd_scan_fwd(dev["x"].float(), dev["dt"], dev["A"], dev["B"], dev["C"])
+
+
+# ---- the state-only pass in segments -------------------------------------------------------
+
+def test_state_pass_segments_match_oracle_and_repeat_bitwise():
+    """8 heads of 163,840 tokens: 10,240 tiles over the grid, so every range is a piece of a
+    chain (about 69 tiles) and the separate state-only pass cuts most pieces into two or three
+    segments, whose local states the last one to finish combines (from h0 for head pieces).
+    Sampled heads (every range boundary of their chains) against the oracle; the combination
+    order is fixed by the plan, so a second call gives the same bits."""
+    inp = workloads.make_shape_inputs(1, 163840, 8, 64, 128, 1, "bf16", seed=41,
+                                      h0_mode="normal", d_mode="normal")
+    dev = to_device(inp)
+    y1, h1 = run_gpu(dev, 256)
+    y2, h2 = run_gpu(dev, 256)
+    assert torch.equal(y1, y2) and torch.equal(h1, h2), "repeated calls differ"
+    check_against_oracle(inp, y1, h1, heads=[(0, 0), (0, 3), (0, 7)], what="segmented state pass")
