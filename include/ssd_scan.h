@@ -94,8 +94,9 @@ size_t ssd_scan_workspace_bytes(const ssd_dims* dims, int chunk_size, int path);
 
 /* How many kernels one ssd_scan_fwd (or ssd_scan_fwd_gated) call enqueues for this problem on
  * the current device, or a negative SSD_ERR_* code.  Chunked path: 3.  Tensor-core path: 1,
- * or 2 for d_state 128 when the sequence is split into more pieces than it has 128-token tiles
- * per CTA (a state-only pass kernel runs first).  A memset of the hand-off flags comes on top. */
+ * or 2 for d_state 128 when the CTAs' ranges of 128-token tiles are no longer than the (batch,
+ * head) chains and some range ends inside a chain: a state-only pass kernel then runs first
+ * (long sequences over few heads).  Memsets of the status word and hand-off flags come on top. */
 int ssd_scan_kernels_per_call(const ssd_dims* dims, int chunk_size, int path);
 
 /*
