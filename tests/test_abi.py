@@ -69,6 +69,16 @@ def test_resolve_path_rules(lib):
     assert m.ssd_scan_resolve_path(dims(), 64, 5) == -1
 
 
+def test_kernels_per_call_without_a_device(lib):
+    """The chunked path's three kernels are fixed; the tensor-core count needs the device's SM
+    count, so without a device it is an error code, as is an invalid problem."""
+    import mamba_ssd_scan_05_b300 as m
+    assert m.ssd_scan_kernels_per_call(dims(dtype=0, P=32, N=16), 64) == 3
+    assert m.ssd_scan_kernels_per_call(dims(dtype=1), 256, m.SSD_PATH_CHUNKED) == 3
+    assert m.ssd_scan_kernels_per_call(dims(H=6, G=4), 64) == -1
+    assert m.ssd_scan_kernels_per_call(dims(N=300), 64) == -2
+
+
 def test_workspace_bytes(lib):
     import mamba_ssd_scan_05_b300 as m
     d = dims(b=2, L=300, H=3, P=5, N=7)
