@@ -395,62 +395,6 @@ __device__ __forceinline__ void fill_dt_slot(DtSlot& sl, const float (&d0)[4], f
 constexpr float kGroupRange2 = 64.f;
 constexpr float kGroupDtMax = 1048576.f;
 
-// A tile's log2 cumsum c2 (4 tokens per lane) by fill_dt_slot's 64-bit fixed-point scan, and
-// (returned, warp-uniform) its last value, the tile's log2 decay.
-__device__ __forceinline__ float tile_scan2(const float (&d0)[4], float A2, int lane,
-                                            float (&c2)[4]) {
-    long long cs[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float a = fminf(fmaxf(d0[i] * A2, -8388608.f), 8388608.f);
-        const long long qa = __float2ll_rn(a * 4294967296.f);
-        cs[i] = i == 0 ? qa : cs[i - 1] + qa;
-    }
-    long long incl = cs[3];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const long long n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-    }
-    long long excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c2[i] = __ll2float_rn(excl + cs[i]) * 2.3283064365386963e-10f;
-    return __shfl_sync(0xffffffffu, c2[3], 31);
-}
-
-// The state-GEMM weights of one tile of a state-only pass (c2, clast2 from tile_scan2), 4 tokens
-// per lane, and (lane 0) its update factors.  grouped (goff = C at the tile's start, <= 0):
-// w_t = 2^-(goff + c2_t) dt_t and, at the group's last tile, H = 2^C_end (H + S_acc),
-// C_end = goff + clast2.  Not grouped (a tile whose own decay exceeds the group range):
-// w_t = 2^(clast2 - c2_t) dt_t, H = 2^clast2 H + S.
-__device__ __forceinline__ void state_weights(float* w_out, float& udec2, float& sigma,
-                                              float& clast2_out, int& sflags_out,
-                                              const float (&d0)[4], const float (&c2)[4],
-                                              float clast2, int lane, bool grouped, float goff,
-                                              int sflags) {
-    float w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        w[i] = (grouped ? ex2(-(goff + c2[i])) : ex2(clast2 - c2[i])) * d0[i];
-    *reinterpret_cast<float4*>(w_out + 4 * lane) = make_float4(w[0], w[1], w[2], w[3]);
-    if (lane == 0) {
-        clast2_out = clast2;
-        sflags_out = sflags;
-        const float u = grouped ? goff + clast2 : clast2;
-        udec2 = u;
-        sigma = grouped ? ex2(u) : 1.f;
-    }
-}
-
-// A tile's largest dt (warp-uniform).
-__device__ __forceinline__ float tile_dtmax(const float (&d0)[4]) {
-    float m = fmaxf(fmaxf(d0[0], d0[1]), fmaxf(d0[2], d0[3]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    return m;
-}
-
 // One 32 x 32 block (rows 32q .. 32q+31, columns 32jb .. 32jb+31) of P = L o G o dt_j for this
 // lane's row: g holds G's block (read from TMEM by the caller); the bf16 pairs go to pk.  Strictly
 // below the diagonal block every L_ij factors exactly as exp(cum_i - m) exp(m - cum_j) with
